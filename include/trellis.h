@@ -1,0 +1,173 @@
+/*
+ * trellis.h -- C ABI of libtrellis: the packed trellis-coded weight matmul on
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The method (pages: @mlx-bun/inference 1.0.0 diff, kernels/trellis/*.ts).
+ * A weight matrix of `rows` x `cols` is stored only as packed codes: each row
+ * is cut into blocks of BT = 256 columns, and each block is a circular
+ * bitstring of BT*k bits (k = 2, 3 or 4 bits per symbol) held in
+ * wpb = BT*k/32 uint32 words, least significant bit first.  Column t of a
+ * block reads the L = 12-bit window that starts at bit (BT-1-t)*k and wraps
+ * from the end of the block to its first word (tiled-prefill.ts, prefill tile
+ * kernel).  The window indexes a 4096-entry f32 codebook, the value is
+ * multiplied by the row's bf16 scale in f32 and rounded to bf16; the decoded
+ * weights are contracted with bf16 activations, accumulated in fp32, and the
+ * result is rounded to bf16.
+ *
+ * Conventions of every entry point:
+ *   - All array arguments are DEVICE pointers of the current CUDA device
+ *     (cudaSetDevice before the call).  bf16 arrays are IEEE bfloat16 bit
+ *     patterns (uint16), row-major.  The caller owns and allocates every
+ *     buffer, inputs, outputs and workspace; the library allocates no memory
+ *     and keeps no pointer after the call returns.
+ *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  Work is
+ *     only enqueued: the call never synchronises.  Results are valid once
+ *     the stream has reached the work.
+ *   - A call returns TRELLIS_OK when its kernels were enqueued.  Any bad
+ *     argument returns an error status before anything is enqueued; no
+ *     kernel traps or asserts.  Kernel-side waits are bounded: a wait that
+ *     gives up records a code readable with trellis_device_status().
+ *   - codes are uint32 [rows, (cols/256)*wpb] (interleave 0).  scales are
+ *     bf16 [rows].  lut is f32 [4096].  codes and x must be 16-byte aligned.
+ */
+#ifndef TRELLIS_H
+#define TRELLIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Geometry of one packed matrix (the pages' TrellisGeometry: axis, T, L, k,
+ * rows, cols, blockInterleave).
+ *   axis 1: rows are output features, cols are input features
+ *           (out[m][r] = sum_c x[m][c] w[r][c]; tiled-prefill.ts).
+ *   axis 0: rows are input features, cols are output features
+ *           (out[m][c] = sum_r x[m][r] w[r][c]; scatter.ts).
+ *   bt must be 256, L must be 12, k in {2, 3, 4}, rows >= 1,
+ *   cols a positive multiple of 256.  interleave must be 0 (contiguous
+ *   blocks; the pages' interleave-2 layout is not accepted).
+ */
+typedef struct trellis_geometry {
+    int32_t axis;
+    int32_t bt;
+    int32_t L;
+    int32_t k;
+    int64_t rows;
+    int64_t cols;
+    int32_t interleave;
+    int32_t reserved;
+} trellis_geometry;
+
+typedef enum trellis_status {
+    TRELLIS_OK = 0,
+    TRELLIS_ERR_NULL = 1,       /* a required pointer is NULL */
+    TRELLIS_ERR_GEOMETRY = 2,   /* bt, L, k, interleave, rows or cols unsupported */
+    TRELLIS_ERR_SHAPE = 3,      /* M or a size out of range, or axis wrong for the call */
+    TRELLIS_ERR_ALIGN = 4,      /* codes, x or workspace not 16-byte aligned */
+    TRELLIS_ERR_WORKSPACE = 5,  /* workspace smaller than trellis_scatter_workspace_bytes() */
+    TRELLIS_ERR_DEVICE = 6,     /* no usable device, or not compute capability 10.3 */
+    TRELLIS_ERR_LAUNCH = 7      /* a kernel launch failed (cudaGetLastError) */
+} trellis_status;
+
+/*
+ * M = 1 decode matvec, axis 1 (the pages' default packed matvec is named but
+ * not shown; its arithmetic follows the prefill tile kernel of
+ * tiled-prefill.ts and the shuffle reduction of wide-prefill.ts).
+ *   x     bf16 [cols]            activations
+ *   out   bf16 [rows]            out[r] = bf16( sum_c x[c] w[r][c] ), fp32 accumulation
+ * Requires g->axis == 1 and cols <= 20480.
+ */
+trellis_status trellis_matvec(const void* x, const uint32_t* codes, const void* scales,
+                              const float* lut, const trellis_geometry* g,
+                              void* out, void* stream);
+
+/*
+ * Axis-1 prefill for 1 <= M <= 32 activation rows (tiled-prefill.ts,
+ * prefill tile kernel; the pages gate it to M = 5..32).  The decoded bf16
+ * weight tile is contracted on the tensor cores (tcgen05, fp32 accumulation
+ * in tensor memory).
+ *   x     bf16 [M, cols]
+ *   out   bf16 [M, rows]         out[m][r] = bf16( sum_c x[m][c] w[r][c] )
+ * Requires g->axis == 1.
+ */
+trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
+                               const void* scales, const float* lut,
+                               const trellis_geometry* g, void* out, void* stream);
+
+/*
+ * Axis-0 scatter for 1 <= M <= 32 activation rows (scatter.ts: scatter
+ * kernels, launch and the sum over splits).  The rows are cut into `splits`
+ * ranges of rp = ceil(rows/splits) rows; range s covers
+ * [s*rp, min(rows, (s+1)*rp)) and may be empty.  fp32 partial sums go to
+ * workspace [M, splits, cols] and a second kernel sums them over the split
+ * axis in split order and rounds to bf16.
+ *   x          bf16 [M, rows]
+ *   splits     1..1024, or 0 for the default of 128
+ *   workspace  f32, at least trellis_scatter_workspace_bytes(g, M, splits) bytes,
+ *              16-byte aligned; contents on entry do not matter
+ *   out        bf16 [M, cols]     out[m][c] = bf16( sum_r x[m][r] w[r][c] )
+ * Requires g->axis == 0.
+ */
+trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
+                               const void* scales, const float* lut,
+                               const trellis_geometry* g, int32_t splits,
+                               float* workspace, size_t workspace_bytes,
+                               void* out, void* stream);
+
+/* M * splits * cols * 4 bytes (splits 0 means 128); 0 for invalid arguments. */
+size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits);
+
+/*
+ * Verification export: decode the whole matrix (vector-expand.ts, expand
+ * kernel).  Never needed on the matmul path.
+ *   w_out    bf16 [rows, cols]    w[r][c] = bf16( f32( lut[win] * scale[r] ) )
+ *   win_out  uint16 [rows, cols]  the window of each weight; may be NULL
+ * Either axis.
+ */
+trellis_status trellis_expand(const uint32_t* codes, const void* scales, const float* lut,
+                              const trellis_geometry* g, void* w_out, uint16_t* win_out,
+                              void* stream);
+
+/*
+ * Glue of a SwiGLU MLP layer built from the packed matmuls (not a step of
+ * the method; the pages only say the prefill input is the RMSNorm output).
+ *   trellis_rmsnorm:  out[m][d] = bf16( x[m][d] / sqrt(mean_d x[m][d]^2 + eps) ),
+ *                     unit gain, fp32 arithmetic; x, out bf16 [M, D], D <= 65536.
+ *   trellis_silu_mul: out[i] = bf16( silu(g[i]) * u[i] ), fp32 arithmetic;
+ *                     g, u, out bf16 [n].
+ */
+trellis_status trellis_rmsnorm(const void* x, int64_t M, int64_t D, float eps,
+                               void* out, void* stream);
+trellis_status trellis_silu_mul(const void* g, const void* u, int64_t n,
+                                void* out, void* stream);
+
+/*
+ * Measurement aid: time-free kernel that performs `iters` rounds of random
+ * 4-byte gathers from a 4096-entry f32 table held in shared memory, on
+ * `blocks` CTAs of 1024 threads, and writes one float per thread to sink
+ * (f32 [blocks*1024]) so that nothing is optimised away.  Timing it with
+ * events gives the shared-memory gather rate that bounds the decode.
+ */
+trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t iters,
+                                    float* sink, void* stream);
+
+/*
+ * Device-side status of the last kernels on the current device: 0 when no
+ * bounded wait gave up.  Copies one word with cudaMemcpy (synchronising the
+ * device) into *status and clears it.  Returns TRELLIS_ERR_NULL or
+ * TRELLIS_ERR_DEVICE on failure.
+ */
+trellis_status trellis_device_status(int32_t* status);
+
+/* Static English text for a status; never NULL. */
+const char* trellis_strerror(trellis_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRELLIS_H */

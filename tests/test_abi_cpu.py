@@ -1,0 +1,120 @@
+"""The C ABI on the host: the library loads, exports every entry point that
+include/trellis.h declares, and rejects bad arguments with the documented
+status before touching the device (CPU only: every call here returns before
+any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from trellis_coded_quantized_gb300 import _lib, geometry
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "trellis.h")
+
+OK, NULL, GEOM, SHAPE, ALIGN, WORKSPACE = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from trellis_coded_quantized_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(trellis_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror(lib):
+    for s in range(8):
+        assert lib.trellis_strerror(s)
+    assert b"unknown" in lib.trellis_strerror(99)
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+A = 0x10000     # aligned fake addresses: never dereferenced, every call below fails validation first
+U = 0x10004     # 4-byte aligned only
+
+
+def test_null_pointers(lib):
+    g = geometry(1, 256, 512, 2)
+    assert lib.trellis_matvec(None, _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == NULL
+    assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), None, _p(A), None) == NULL
+    assert lib.trellis_prefill(_p(A), 8, _p(A), None, _p(A), ctypes.byref(g), _p(A), None) == NULL
+    g0 = geometry(0, 512, 256, 3)
+    assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, None, 1 << 20, _p(A), None) == NULL
+    assert lib.trellis_expand(_p(A), _p(A), _p(A), ctypes.byref(g), None, None, None) == NULL
+    assert lib.trellis_device_status(None) == NULL
+
+
+@pytest.mark.parametrize("field,value", [("bt", 128), ("L", 11), ("k", 1), ("k", 5), ("interleave", 2),
+                                         ("cols", 300), ("cols", 0), ("rows", 0), ("axis", 2)])
+def test_bad_geometry(lib, field, value):
+    g = geometry(1, 256, 512, 2)
+    setattr(g, field, value)
+    st = lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None)
+    assert st == GEOM
+    assert lib.trellis_expand(_p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None, None) == GEOM
+
+
+def test_axis_must_match_entry_point(lib):
+    g1 = geometry(1, 256, 512, 2)
+    g0 = geometry(0, 256, 512, 2)
+    assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(g0), _p(A), None) == SHAPE
+    assert lib.trellis_prefill(_p(A), 8, _p(A), _p(A), _p(A), ctypes.byref(g0), _p(A), None) == SHAPE
+    assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g1), 0, _p(A), 1 << 30, _p(A), None) == SHAPE
+
+
+def test_sizes_out_of_range(lib):
+    g1 = geometry(1, 256, 512, 2)
+    for M in (0, 33, -1):
+        assert lib.trellis_prefill(_p(A), M, _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == SHAPE
+    wide = geometry(1, 256, 20480 + 256, 4)
+    assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(wide), _p(A), None) == SHAPE
+    g0 = geometry(0, 512, 256, 3)
+    for M, s in ((0, 0), (33, 0), (1, -1), (1, 1025)):
+        assert lib.trellis_scatter(_p(A), M, _p(A), _p(A), _p(A), ctypes.byref(g0), s, _p(A), 1 << 30, _p(A), None) == SHAPE
+
+
+def test_misaligned(lib):
+    g1 = geometry(1, 256, 512, 2)
+    assert lib.trellis_matvec(_p(U), _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    assert lib.trellis_matvec(_p(A), _p(U), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    assert lib.trellis_prefill(_p(A), 5, _p(U), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    g0 = geometry(0, 512, 256, 3)
+    assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, _p(U), 1 << 30, _p(A), None) == ALIGN
+
+
+def test_workspace_size(lib):
+    g0 = geometry(0, 17408, 5120, 3)
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 1, 0) == 1 * 128 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 64) == 4 * 64 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 0, 0) == 0
+    bad = geometry(0, 17408, 5000, 3)
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(bad), 1, 0) == 0
+    need = 1 * 128 * 5120 * 4
+    assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, _p(A), need - 4, _p(A), None) == WORKSPACE
+
+
+def test_glue_validation(lib):
+    assert lib.trellis_rmsnorm(None, 1, 16, ctypes.c_float(1e-6), _p(A), None) == NULL
+    assert lib.trellis_rmsnorm(_p(A), 1, 70000, ctypes.c_float(1e-6), _p(A), None) == SHAPE
+    assert lib.trellis_silu_mul(_p(A), _p(A), 0, _p(A), None) == SHAPE
+    assert lib.trellis_gather_probe(_p(A), 0, 1, _p(A), None) == SHAPE
+    assert lib.trellis_gather_probe(_p(U), 1, 1, _p(A), None) == ALIGN

@@ -1,0 +1,258 @@
+"""CUDA path (through the C ABI) against the oracle, element by element.
+
+Decoded windows and weights must be bit-exact; contractions must satisfy
+|gpu - y| <= 4e-3 * sum|x*w| + 1 bf16 ulp per element (y, sum|x*w| from the
+oracle in double).  Probes with unit vectors and integer codebooks must come
+back bit-exact through every fused kernel.
+"""
+import numpy as np
+import pytest
+
+import trellis_coded_quantized_gb300 as tcq
+from trellis_coded_quantized_gb300 import synth
+from gpu_util import check_close, dev, host_bf16, on_device
+from conftest import has_gpu
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not has_gpu(), reason="needs a CUDA GPU")]
+
+ONE = 0x3F80  # bf16 1.0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from trellis_coded_quantized_gb300 import build
+    build.build()
+
+
+def _oracle_axis1(orc, p):
+    W, _ = orc.expand(p["codes"], p["rows"], p["cols"], p["k"], p["scales"], p["lut"])
+    y, a, _ = orc.matmul_axis1(p["x"], W)
+    return W, y, a
+
+
+def _oracle_axis0(orc, p, splits=0):
+    W, _ = orc.expand(p["codes"], p["rows"], p["cols"], p["k"], p["scales"], p["lut"])
+    y, a, _, part = orc.matmul_axis0(p["x"], W, splits)
+    return W, y, a, part
+
+
+# ----------------------------------------------------------------- expand
+
+@pytest.mark.parametrize("axis,rows,cols,k", [
+    (1, 256, 512, 2),        # tiny matvec geometry
+    (1, 17408, 5120, 4),     # decode matvec geometry
+    (1, 17408, 5120, 2),     # prefill geometries
+    (1, 17408, 5120, 3),
+    (0, 17408, 5120, 3),     # axis-0 scatter geometry
+    (1, 1, 256, 4),          # one block, one row
+    (0, 37, 768, 3),         # ragged rows, odd block count
+])
+def test_expand_bit_exact(orc, axis, rows, cols, k):
+    p = synth.problem(axis, 1, rows, cols, k, seed=0)
+    d = on_device(p)
+    w, win = tcq.trellis_expand(d["codes"], d["scales"], d["lut"], d["g"], with_windows=True)
+    ow, owin = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    assert np.array_equal(host_bf16(win), owin), "windows differ"
+    assert np.array_equal(host_bf16(w), ow), "decoded weights differ"
+
+
+# ----------------------------------------------------------------- matvec
+
+@pytest.mark.parametrize("rows,cols,k", [
+    (256, 512, 2),           # tiny axis-1 matvec, seed 0
+    (17408, 5120, 4),        # decode matvec, full size
+    (17408, 5120, 3),
+    (17408, 5120, 2),
+    (1, 256, 4), (3, 256, 3), (37, 768, 2), (1000, 1280, 3),
+    (4099, 20480, 4),        # widest input the kernel takes
+    (152 * 3 + 5, 2304, 2),  # rows not a multiple of the grid
+])
+def test_matvec(orc, rows, cols, k):
+    p = synth.problem(1, 1, rows, cols, k, seed=0)
+    d = on_device(p)
+    out = tcq.trellis_matvec(d["x"][0], d["codes"], d["scales"], d["lut"], d["g"])
+    _, y, a = _oracle_axis1(orc, p)
+    check_close(orc, host_bf16(out)[None, :], y, a, f"matvec {rows}x{cols} k={k}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_matvec_unit_vectors_exact(orc, k):
+    rows, cols = 300, 1024
+    p = synth.problem(1, 1, rows, cols, k, seed=3)
+    d = on_device(p)
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    for c in (0, 1, 2, 127, 255, 256, 511, 1023):
+        e = np.zeros(cols, np.uint16)
+        e[c] = ONE
+        out = tcq.trellis_matvec(dev(e), d["codes"], d["scales"], d["lut"], d["g"])
+        assert np.array_equal(host_bf16(out), W[:, c]), c
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_matvec_lut_readback_exact(orc, k):
+    """lut[v] = v & 255 and v >> 8 with unit scales return every window."""
+    rows, cols = 200, 768
+    p = synth.problem(1, 1, rows, cols, k, seed=4)
+    _, win = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    v = np.arange(4096)
+    d = on_device(p)
+    sc1 = dev(np.full(rows, ONE, np.uint16))
+    lo, hi = dev((v & 255).astype(np.float32)), dev((v >> 8).astype(np.float32))
+    for c in (0, 1, 4, 200, 255, 256, 767):
+        e = np.zeros(cols, np.uint16)
+        e[c] = ONE
+        a = host_bf16(tcq.trellis_matvec(dev(e), d["codes"], sc1, lo, d["g"]))
+        b = host_bf16(tcq.trellis_matvec(dev(e), d["codes"], sc1, hi, d["g"]))
+        from oracle import bf16_to_float
+        got = bf16_to_float(a).astype(np.int64) + 256 * bf16_to_float(b).astype(np.int64)
+        assert np.array_equal(got, win[:, c].astype(np.int64)), c
+
+
+# ----------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 16, 17, 31, 32])
+def test_prefill_small(orc, M, k):
+    rows, cols = 300, 768          # 3 CTAs with a ragged last one; 3 blocks (odd: both stages, parity flips)
+    p = synth.problem(1, M, rows, cols, k, seed=5)
+    d = on_device(p)
+    out = tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"])
+    _, y, a = _oracle_axis1(orc, p)
+    check_close(orc, host_bf16(out), y, a, f"prefill M={M} k={k}")
+    assert tcq.trellis_device_status() == 0
+
+
+@pytest.mark.parametrize("M,k", [(32, 4), (5, 2), (16, 3), (8, 4), (32, 2), (32, 3)])
+def test_prefill_full_size(orc, M, k):
+    rows, cols = 17408, 5120
+    p = synth.problem(1, M, rows, cols, k, seed=0)
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"]))
+    if (M, k) in ((32, 4), (5, 2)):
+        _, y, a = _oracle_axis1(orc, p)
+        check_close(orc, out, y, a, f"prefill full M={M} k={k}")
+    else:
+        rng = np.random.default_rng(M * 10 + k)
+        ms = rng.integers(0, M, 4000)
+        js = rng.integers(0, rows, 4000)
+        y, a = orc.sample(p["x"], p["codes"], rows, cols, k, p["scales"], p["lut"], 1, ms, js)
+        check_close(orc, out[ms, js], y, a, f"prefill full sampled M={M} k={k}")
+    assert tcq.trellis_device_status() == 0
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_prefill_unit_vectors_exact(orc, k):
+    rows, cols, M = 260, 1024, 8
+    p = synth.problem(1, M, rows, cols, k, seed=6)
+    d = on_device(p)
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    cs = [0, 1, 255, 256, 300, 511, 512, 1023]
+    e = np.zeros((M, cols), np.uint16)
+    for m, c in enumerate(cs):
+        e[m, c] = ONE
+    out = host_bf16(tcq.trellis_prefill(dev(e), d["codes"], d["scales"], d["lut"], d["g"]))
+    for m, c in enumerate(cs):
+        assert np.array_equal(out[m], W[:, c]), (m, c)
+
+
+# ----------------------------------------------------------------- scatter
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_scatter_full_size(orc, M):
+    rows, cols, k = 17408, 5120, 3
+    p = synth.problem(0, M, rows, cols, k, seed=0)
+    d = on_device(p)
+    out = tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128)
+    _, y, a, _ = _oracle_axis0(orc, p)
+    check_close(orc, host_bf16(out), y, a, f"scatter full M={M}")
+
+
+@pytest.mark.parametrize("rows,cols,k,M,splits", [
+    (1, 256, 3, 1, 0), (7, 256, 2, 2, 0), (300, 1280, 4, 3, 7), (300, 1280, 3, 5, 1),
+    (300, 768, 2, 9, 1024), (513, 2048, 3, 4, 128), (129, 256, 4, 32, 64), (64, 5120, 3, 1, 128),
+])
+def test_scatter_small(orc, rows, cols, k, M, splits):
+    p = synth.problem(0, M, rows, cols, k, seed=7)
+    d = on_device(p)
+    out = tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=splits)
+    _, y, a, _ = _oracle_axis0(orc, p)
+    check_close(orc, host_bf16(out), y, a, f"scatter {rows}x{cols} k={k} M={M} S={splits}")
+
+
+def test_scatter_partials(orc):
+    """The fp32 partial of every split against the oracle's split sums; empty
+    splits past the last row hold zeros."""
+    import torch
+    rows, cols, k, M, S = 100, 512, 3, 2, 48      # rp = 3: splits 34..47 are empty
+    p = synth.problem(0, M, rows, cols, k, seed=8)
+    d = on_device(p)
+    ws = torch.zeros(tcq.trellis_scatter_workspace_bytes(d["g"], M, S) // 4, dtype=torch.float32, device="cuda")
+    ws.fill_(float("nan"))
+    tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=S, workspace=ws)
+    part = ws.view(M, S, cols).cpu().numpy().astype(np.float64)
+    W, _, _, ref = _oracle_axis0(orc, p, S)
+    from oracle import bf16_to_float
+    xf = np.abs(bf16_to_float(p["x"]).astype(np.float64))
+    wf = np.abs(bf16_to_float(W).astype(np.float64))
+    rp = -(-rows // S)
+    for s in range(S):
+        r0, r1 = s * rp, min(rows, (s + 1) * rp)
+        if r0 >= r1:
+            assert np.all(part[:, s, :] == 0.0), s
+            continue
+        asum = xf[:, r0:r1] @ wf[r0:r1]
+        assert np.all(np.abs(part[:, s, :] - ref[:, s, :]) <= 1e-5 * asum + 1e-30), s
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_scatter_unit_vectors_exact(orc, k):
+    rows, cols = 200, 1024
+    p = synth.problem(0, 1, rows, cols, k, seed=9)
+    d = on_device(p)
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    for r in (0, 1, 99, 199):
+        e = np.zeros((1, rows), np.uint16)
+        e[0, r] = ONE
+        out = host_bf16(tcq.trellis_scatter(dev(e), d["codes"], d["scales"], d["lut"], d["g"]))
+        assert np.array_equal(out[0], W[r]), r
+
+
+# ----------------------------------------------------------------- glue
+
+def _ulps(a, b):
+    from oracle import bf16_to_float
+    fa, fb = bf16_to_float(a).astype(np.float64), bf16_to_float(b).astype(np.float64)
+    from oracle import bf16_ulp
+    return np.abs(fa - fb) / bf16_ulp(np.maximum(np.abs(fa), np.abs(fb)))
+
+
+def test_rmsnorm(orc):
+    x = synth.activations(11, 16, 5120)
+    out = host_bf16(tcq.trellis_rmsnorm(dev(x), 1e-6))
+    assert np.all(_ulps(out, orc.rmsnorm(x, 1e-6)) <= 1.0)
+
+
+def test_silu_mul(orc):
+    g = synth.activations(12, 4, 17408)
+    u = synth.activations(13, 4, 17408)
+    out = host_bf16(tcq.trellis_silu_mul(dev(g), dev(u)))
+    assert np.all(_ulps(out, orc.silu_mul(g, u)) <= 1.0)
+
+
+# ----------------------------------------------------------------- errors on a live device
+
+def test_errors_do_not_launch():
+    import torch
+    p = synth.problem(1, 1, 256, 512, 2, seed=0)
+    d = on_device(p)
+    bad = tcq.geometry(1, 256, 512, 2)
+    bad.L = 11
+    with pytest.raises(tcq.TrellisError, match="GEOMETRY"):
+        tcq.trellis_matvec(d["x"][0], d["codes"], d["scales"], d["lut"], bad)
+    g0 = tcq.geometry(0, 256, 512, 2)
+    x0 = dev(synth.activations(0, 1, 256))
+    small = torch.empty(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(tcq.TrellisError, match="WORKSPACE"):
+        tcq.trellis_scatter(x0, d["codes"], d["scales"], d["lut"], g0, workspace=small)
+    torch.cuda.synchronize()
+    assert tcq.trellis_device_status() == 0

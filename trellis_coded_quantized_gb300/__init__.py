@@ -1,0 +1,191 @@
+"""GB300-native packed trellis-coded weight matmul.
+
+Python binding of libtrellis (C ABI: include/trellis.h).  Each function has
+the name of the C entry point it calls and only marshals arguments: PyTorch
+CUDA tensors in, device pointers out; every step of the computation runs in
+the library's CUDA kernels.  bf16 tensors may be torch.bfloat16 or int16 /
+uint16 holding bf16 bit patterns.
+
+A packed matrix is described by ``geometry(axis, rows, cols, k)``:
+  axis 1: rows are output features, cols input features (x [M, cols] -> [M, rows])
+  axis 0: rows are input features, cols output features (x [M, rows] -> [M, cols])
+codes uint32 (int32 storage) [rows, (cols/256)*256*k/32], scales bf16 [rows],
+lut float32 [4096].
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+
+BT = 256
+L = 12
+DEFAULT_SPLITS = 128
+
+
+class TrellisError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.load().trellis_strerror(status).decode()
+        super().__init__(f"{where}: {_lib.STATUS.get(status, status)}: {msg}")
+
+
+def geometry(axis: int, rows: int, cols: int, k: int, interleave: int = 0) -> _lib.Geometry:
+    return _lib.Geometry(axis, BT, L, k, rows, cols, interleave, 0)
+
+
+def words_per_row(cols: int, k: int) -> int:
+    return (cols // BT) * (BT * k // 32)
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise TrellisError(status, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev(t, name: str, dtypes, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_types():
+    torch = _torch()
+    return (torch.bfloat16, torch.int16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
+
+
+def _code_types():
+    torch = _torch()
+    return (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _packed(codes, scales, lut, g):
+    torch = _torch()
+    return (_dev(codes, "codes", _code_types(), (g.rows, words_per_row(g.cols, g.k))),
+            _dev(scales, "scales", _bf16_types(), (g.rows,)),
+            _dev(lut, "lut", (torch.float32,), (1 << L,)))
+
+
+def _out(out, shape, like):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=like.device)
+    return out
+
+
+def trellis_matvec(x, codes, scales, lut, g, out=None, stream=None):
+    """M = 1, axis 1: x bf16 [cols] (or [1, cols]) -> out bf16 [rows]."""
+    c, s, t = _packed(codes, scales, lut, g)
+    xp = _dev(x, "x", _bf16_types())
+    if x.numel() != g.cols:
+        raise ValueError("x must hold cols elements")
+    out = _out(out, (g.rows,), x)
+    op = _dev(out, "out", _bf16_types())
+    if out.numel() != g.rows:
+        raise ValueError("out must hold rows elements")
+    _check(_lib.load().trellis_matvec(xp, c, s, t, ctypes.byref(g), op, _stream(stream)), "trellis_matvec")
+    return out
+
+
+def trellis_prefill(x, codes, scales, lut, g, out=None, stream=None):
+    """Axis 1, 1 <= M <= 32: x bf16 [M, cols] -> out bf16 [M, rows]."""
+    c, s, t = _packed(codes, scales, lut, g)
+    M = x.shape[0]
+    xp = _dev(x, "x", _bf16_types(), (M, g.cols))
+    out = _out(out, (M, g.rows), x)
+    op = _dev(out, "out", _bf16_types(), (M, g.rows))
+    _check(_lib.load().trellis_prefill(xp, M, c, s, t, ctypes.byref(g), op, _stream(stream)), "trellis_prefill")
+    return out
+
+
+def trellis_scatter_workspace_bytes(g, M: int, splits: int = 0) -> int:
+    return int(_lib.load().trellis_scatter_workspace_bytes(ctypes.byref(g), M, splits))
+
+
+def trellis_scatter(x, codes, scales, lut, g, splits: int = 0, workspace=None, out=None, stream=None):
+    """Axis 0, 1 <= M <= 32: x bf16 [M, rows] -> out bf16 [M, cols] via fp32
+    split partials in `workspace` (float32, allocated here when None)."""
+    torch = _torch()
+    c, s, t = _packed(codes, scales, lut, g)
+    M = x.shape[0]
+    xp = _dev(x, "x", _bf16_types(), (M, g.rows))
+    need = trellis_scatter_workspace_bytes(g, M, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4) // 4, dtype=torch.float32, device=x.device)
+    wp = _dev(workspace, "workspace", (torch.float32,))
+    out = _out(out, (M, g.cols), x)
+    op = _dev(out, "out", _bf16_types(), (M, g.cols))
+    _check(_lib.load().trellis_scatter(xp, M, c, s, t, ctypes.byref(g), splits, wp,
+                                       workspace.numel() * 4, op, _stream(stream)), "trellis_scatter")
+    return out
+
+
+def trellis_expand(codes, scales, lut, g, w_out=None, win_out=None, with_windows=False, stream=None):
+    """Decode the packed matrix: w bf16 [rows, cols] (and windows int16 [rows, cols])."""
+    torch = _torch()
+    c, s, t = _packed(codes, scales, lut, g)
+    if w_out is None:
+        w_out = torch.empty((g.rows, g.cols), dtype=torch.bfloat16, device=codes.device)
+    wp = _dev(w_out, "w_out", _bf16_types(), (g.rows, g.cols))
+    if win_out is None and with_windows:
+        win_out = torch.empty((g.rows, g.cols), dtype=torch.int16, device=codes.device)
+    vp = None if win_out is None else _dev(win_out, "win_out", _bf16_types(), (g.rows, g.cols))
+    _check(_lib.load().trellis_expand(c, s, t, ctypes.byref(g), wp, vp, _stream(stream)), "trellis_expand")
+    return (w_out, win_out) if win_out is not None else w_out
+
+
+def trellis_rmsnorm(x, eps: float = 1e-6, out=None, stream=None):
+    M, D = x.shape
+    xp = _dev(x, "x", _bf16_types(), (M, D))
+    out = _out(out, (M, D), x)
+    op = _dev(out, "out", _bf16_types(), (M, D))
+    _check(_lib.load().trellis_rmsnorm(xp, M, D, eps, op, _stream(stream)), "trellis_rmsnorm")
+    return out
+
+
+def trellis_silu_mul(g_, u, out=None, stream=None):
+    gp = _dev(g_, "g", _bf16_types())
+    up = _dev(u, "u", _bf16_types(), tuple(g_.shape))
+    out = _out(out, tuple(g_.shape), g_)
+    op = _dev(out, "out", _bf16_types(), tuple(g_.shape))
+    _check(_lib.load().trellis_silu_mul(gp, up, g_.numel(), op, _stream(stream)), "trellis_silu_mul")
+    return out
+
+
+def trellis_gather_probe(lut, blocks: int, iters: int, sink=None, stream=None):
+    torch = _torch()
+    lp = _dev(lut, "lut", (torch.float32,), (1 << L,))
+    if sink is None:
+        sink = torch.empty(blocks * 1024, dtype=torch.float32, device=lut.device)
+    sp = _dev(sink, "sink", (torch.float32,), (blocks * 1024,))
+    _check(_lib.load().trellis_gather_probe(lp, blocks, iters, sp, _stream(stream)), "trellis_gather_probe")
+    return sink
+
+
+def trellis_device_status() -> int:
+    v = ctypes.c_int32(0)
+    _check(_lib.load().trellis_device_status(ctypes.byref(v)), "trellis_device_status")
+    return int(v.value)
+
+
+def trellis_strerror(status: int) -> str:
+    return _lib.load().trellis_strerror(status).decode()

@@ -1,0 +1,99 @@
+// Device primitives shared by the libtrellis kernels (sm_103a).
+//
+// A "unit" is 32 consecutive symbol slots of one block, starting on a word
+// boundary: unit u (0..7) of a block holds block bits [32uk, 32uk + 32k), i.e.
+// words [u*k, u*k + k).  Window i (0..31) of the unit starts at unit-local bit
+// k*i and belongs to block column t = 255 - 32u - i (the window of column t
+// starts at block bit (BT-1-t)*k: @mlx-bun/inference 1.0.0,
+// kernels/trellis/tiled-prefill.ts, prefill tile kernel).  The last window
+// spills into the first word of the next unit of the same block, and unit 7
+// spills into unit 0 (the tail-biting wrap to word 0 of the block).  A unit
+// therefore needs its k words plus one neighbour word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace tcq {
+
+constexpr int kBT = 256;        // block length in columns
+constexpr int kL = 12;          // window bits
+constexpr int kLutN = 1 << kL;  // codebook entries
+constexpr int kUnitsPerBlock = kBT / 32;
+
+// Byte offset 4*win of window i of a unit held in w[0..K] (w[K] = neighbour).
+// The shift is taken two bits early so the masked value is the table offset.
+// With i a compile-time constant after unrolling, this is one funnel shift and
+// one AND.
+template <int K>
+__device__ __forceinline__ uint32_t win_off(const uint32_t* w, int i) {
+    const int b = K * i;
+    const int q = b >> 5;
+    const int s = b & 31;
+    uint32_t f;
+    if (s >= 2)
+        f = __funnelshift_r(w[q], w[q + 1], s - 2);
+    else if (q > 0)
+        f = __funnelshift_r(w[q - 1], w[q], 30 + s);
+    else
+        f = w[0] << (2 - s);
+    return f & 0x3FFCu;
+}
+
+__device__ __forceinline__ float lut_at(const float* lut_s, uint32_t byte_off) {
+    return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(lut_s) + byte_off);
+}
+
+// Stage the 4096-entry codebook in shared memory (16 KB, float4 copies).
+__device__ __forceinline__ void stage_lut(float* lut_s, const float* __restrict__ lut) {
+    const float4* src = reinterpret_cast<const float4*>(lut);
+    float4* dst = reinterpret_cast<float4*>(lut_s);
+    for (int i = threadIdx.x; i < kLutN / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+// Streaming loads of code words: read once, so they skip L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint32_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const uint32_t* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// The K words of one unit at p (16-byte aligned for K=4, 8-byte for K=2).
+template <int K>
+__device__ __forceinline__ void load_unit(uint32_t* w, const uint32_t* p) {
+    if constexpr (K == 4) {
+        const uint4 v = ld_stream_v4(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (K == 2) {
+        const uint2 v = ld_stream_v2(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        #pragma unroll
+        for (int j = 0; j < K; ++j) w[j] = ld_stream(p + j);
+    }
+}
+
+// Lane that holds the first word of the next unit of the same block, when
+// the 8 units of a block sit on 8 consecutive lanes (unit 7 wraps to unit 0).
+__device__ __forceinline__ int next_unit_lane(int lane) {
+    return (lane & ~7) | ((lane + 1) & 7);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
+    return __uint_as_float(h16 << 16);
+}
+
+}  // namespace tcq

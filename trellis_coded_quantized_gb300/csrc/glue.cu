@@ -1,0 +1,91 @@
+// Glue of a SwiGLU MLP layer (RMSNorm, silu * up) and the shared-memory
+// gather probe.  None of this is a step of the trellis method.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tcq {
+namespace {
+
+// One CTA per activation row: fp32 sum of squares, then x * rsqrt(mean + eps).
+__global__ void __launch_bounds__(256)
+rmsnorm_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* __restrict__ out) {
+    __shared__ float part[8];
+    const uint16_t* xr = x + (int64_t)blockIdx.x * D;
+    uint16_t* orow = out + (int64_t)blockIdx.x * D;
+    float ss = 0.f;
+    for (int64_t d = threadIdx.x; d < D; d += blockDim.x) {
+        const float v = bf16_bits_to_float(xr[d]);
+        ss = fmaf(v, v, ss);
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+    for (int64_t d = threadIdx.x; d < D; d += blockDim.x)
+        orow[d] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(xr[d]) * inv));
+}
+
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
+                                int64_t n, uint16_t* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float gv = bf16_bits_to_float(g[i]);
+        const float uv = bf16_bits_to_float(u[i]);
+        out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv));
+    }
+}
+
+// Random 4-byte gathers from a 4096-entry shared-memory table: 8 independent
+// xorshift streams per thread, one gather per draw.  Each draw costs a few
+// integer operations, well under what the shared-memory port needs, so the
+// kernel runs at the gather rate of the SM.
+__global__ void __launch_bounds__(1024, 1)
+gather_probe_kernel(const float* __restrict__ lut, int iters, float* __restrict__ sink) {
+    __shared__ __align__(16) float lut_s[kLutN];
+    stage_lut(lut_s, lut);
+    __syncthreads();
+    uint32_t st[8];
+    const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    #pragma unroll
+    for (int j = 0; j < 8; ++j) st[j] = 0x9E3779B9u * (tid * 8u + j + 1u);
+    float acc = 0.f;
+    for (int it = 0; it < iters; ++it) {
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            st[j] ^= st[j] << 13;
+            st[j] ^= st[j] >> 17;
+            st[j] ^= st[j] << 5;
+            acc += lut_at(lut_s, st[j] & 0x3FFCu);
+        }
+    }
+    sink[tid] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int64_t M, int64_t D, float eps,
+                           uint16_t* out, cudaStream_t stream) {
+    rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(x, D, eps, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
+                            uint16_t* out, cudaStream_t stream) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    silu_mul_kernel<<<(unsigned)blocks, 256, 0, stream>>>(g, u, n, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, float* sink,
+                                cudaStream_t stream) {
+    gather_probe_kernel<<<(unsigned)blocks, 1024, 0, stream>>>(lut, iters, sink);
+    return cudaGetLastError();
+}
+
+}  // namespace tcq

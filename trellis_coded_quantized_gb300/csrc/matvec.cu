@@ -1,0 +1,175 @@
+// trellis_matvec: M = 1 axis-1 packed matvec, out[r] = bf16(sum_c x[c] w[r][c]).
+//
+// Arithmetic: the decoded weight is bf16(f32(lut[win] * scale[r])) and the
+// dot product accumulates in fp32 (@mlx-bun/inference 1.0.0,
+// kernels/trellis/tiled-prefill.ts, prefill tile kernel; the pages name the
+// default M=1 matvec without showing it, and wide-prefill.ts shows the
+// shuffle reduction of per-lane partial sums).
+//
+// GB300 layout of the work (warp FMA, no tensor cores at M = 1):
+//   - one CTA per SM, up to 640 threads, the 16 KB codebook in shared memory;
+//   - a "row group" of TG threads covers one whole row: thread t owns the
+//     32-column unit t of every row and keeps those 32 activations in
+//     registers as f32 for the whole kernel, so x is read once per CTA;
+//   - per row, a thread streams its unit's k words (one 16/8-byte load, or
+//     three 4-byte loads at k=3, coalesced across the warp), takes the
+//     neighbour word from the next lane with __shfl_sync, and does 32
+//     window extractions, codebook gathers, scale multiplies, bf16 roundings
+//     and FMAs;
+//   - RB rows are accumulated side by side, then a butterfly reduce-scatter
+//     over the warp (RB-1+... shuffles for RB rows) and a sum over the warps
+//     of the group in shared memory produce the RB outputs.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tcq {
+namespace {
+
+constexpr int kMvThreads = 640;
+constexpr int kRB = 16;  // rows per reduction batch (power of two, <= 32)
+
+// Butterfly reduce-scatter of a[0..RB) over the 32 lanes: afterwards a[0] of
+// lane l holds the warp sum of row (l >> (5 - log2 RB)) & (RB - 1).
+template <int N>
+__device__ __forceinline__ void rs_stage(float* a, int lane, int off) {
+    const bool upper = (lane & off) != 0;
+    #pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float send = upper ? a[j] : a[j + N];
+        const float keep = upper ? a[j + N] : a[j];
+        a[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+}
+
+__device__ __forceinline__ float reduce_scatter16(float* a, int lane) {
+    rs_stage<8>(a, lane, 16);
+    rs_stage<4>(a, lane, 8);
+    rs_stage<2>(a, lane, 4);
+    rs_stage<1>(a, lane, 2);
+    a[0] += __shfl_xor_sync(0xffffffffu, a[0], 1);
+    return a[0];
+}
+
+template <int K>
+__global__ void __launch_bounds__(kMvThreads, 1)
+matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
+              const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+              int rows, int units, int tg, int ng, uint16_t* __restrict__ out) {
+    extern __shared__ __align__(16) float smem[];
+    float* lut_s = smem;
+    const int wg = tg >> 5;                       // warps per row group
+    float* red = smem + kLutN;                    // [2][ng][wg][kRB]
+    stage_lut(lut_s, lut);
+
+    const int g = threadIdx.x / tg;
+    const int t = threadIdx.x - g * tg;
+    const int lane = threadIdx.x & 31;
+    const int wig = t >> 5;
+    const bool active = t < units;
+    const int64_t wpr = (int64_t)units * K;
+
+    // activations of this thread's unit: window i <-> column c0 + 31 - i
+    float xf[32];
+    if (active) {
+        const int c0 = (t >> 3) * kBT + (224 - 32 * (t & 7));
+        const uint4* xp = reinterpret_cast<const uint4*>(x + c0);
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(xp + q);
+            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xf[31 - (8 * q + 2 * j)] = bf16_bits_to_float(e[j] & 0xFFFFu);
+                xf[31 - (8 * q + 2 * j + 1)] = bf16_bits_to_float(e[j] >> 16);
+            }
+        }
+    } else {
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) xf[i] = 0.f;
+    }
+    __syncthreads();
+
+    const int r0 = (int)((int64_t)rows * blockIdx.x / gridDim.x);
+    const int r1 = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
+    const int per_group = (r1 - r0 + ng - 1) / ng;
+    const int src = next_unit_lane(lane);
+    const uint32_t* tp = codes + (int64_t)t * K;
+
+    int buf = 0;
+    for (int j0 = 0; j0 < per_group; j0 += kRB, buf ^= 1) {
+        float acc[kRB];
+        uint32_t nxt[K];
+        {
+            const int row = r0 + g + ng * j0;
+            if (active && row < r1) load_unit<K>(nxt, tp + (int64_t)row * wpr);
+            else {
+                #pragma unroll
+                for (int j = 0; j < K; ++j) nxt[j] = 0u;
+            }
+        }
+        #pragma unroll
+        for (int rho = 0; rho < kRB; ++rho) {
+            const int row = r0 + g + ng * (j0 + rho);
+            uint32_t w[K + 1];
+            #pragma unroll
+            for (int j = 0; j < K; ++j) w[j] = nxt[j];
+            // prefetch the next row of the batch
+            if (rho + 1 < kRB) {
+                const int rn = row + ng;
+                if (active && rn < r1) load_unit<K>(nxt, tp + (int64_t)rn * wpr);
+            }
+            acc[rho] = 0.f;
+            if (row < r1) {                              // uniform over the row group
+                w[K] = __shfl_sync(0xffffffffu, w[0], src);
+                const float s = bf16_bits_to_float(__ldg(scales + row));
+                float a0 = 0.f, a1 = 0.f;
+                #pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float v0 = lut_at(lut_s, win_off<K>(w, i));
+                    const float v1 = lut_at(lut_s, win_off<K>(w, i + 1));
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(v0, s), __fmul_rn(v1, s));
+                    a0 = fmaf(__low2float(h), xf[i], a0);
+                    a1 = fmaf(__high2float(h), xf[i + 1], a1);
+                }
+                acc[rho] = a0 + a1;
+            }
+        }
+        // rows of this batch: warp reduce-scatter, then sum the warps of the group
+        const float v = reduce_scatter16(acc, lane);
+        float* rb = red + (size_t)buf * ng * wg * kRB;
+        if ((lane & 1) == 0) rb[((size_t)g * wg + wig) * kRB + ((lane >> 1) & 15)] = v;
+        __syncthreads();
+        if (t < kRB) {
+            const int row = r0 + g + ng * (j0 + t);
+            if (row < r1) {
+                float s = 0.f;
+                for (int w = 0; w < wg; ++w) s += rb[((size_t)g * wg + w) * kRB + t];
+                out[row] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+            }
+        }
+        // the other buffer is written next; one barrier per batch suffices
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
+                          int sm_count, cudaStream_t stream) {
+    const int units = (int)(p.cols / 32);
+    const int tg = ((units + 31) / 32) * 32;
+    if (tg > kMvThreads) return cudaErrorInvalidValue;
+    int ng = kMvThreads / tg;
+    const int threads = tg * ng;
+    int grid = sm_count;
+    if ((int64_t)grid > p.rows) grid = (int)p.rows;
+    const size_t smem = (size_t)(kLutN + 2 * ng * (tg / 32) * kRB) * sizeof(float);
+    switch (p.k) {
+        case 2: matvec_kernel<2><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
+        case 3: matvec_kernel<3><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
+        case 4: matvec_kernel<4><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tcq

@@ -1,0 +1,210 @@
+// trellis_scatter: axis-0 packed matmul, out[m][c] = bf16(sum_r x[m][r] w[r][c]).
+//
+// The rows (input features) are cut into `splits` ranges of rp = ceil(R/S)
+// rows; each range's fp32 partial sums go to partial[m][s][c] and a second
+// kernel sums them over s (@mlx-bun/inference 1.0.0, kernels/trellis/
+// scatter.ts: scatter kernels, rowsPer/r0/r1 split ranges, the [M, SPLITS,
+// C] float partials and their sum over the split axis, cast to bf16).
+//
+// GB300 layout of the work:
+//   - a lane owns one 32-column unit of the output columns and walks the rows
+//     of its split: per row it streams the unit's k words (coalesced over the
+//     warp: 32 lanes cover 4 consecutive blocks), takes the neighbour word
+//     by __shfl_sync, decodes 32 weights and does MB FMAs per weight, one per
+//     activation row (the shared-M variants of scatter.ts share each decoded
+//     weight across activation rows the same way);
+//   - the 4 warps of a CTA take interleaved rows of the same (split, column
+//     range) and their partial sums are added in shared memory before the
+//     store, so a CTA writes one [MB, 1024] slab of partials;
+//   - more than 4 activation rows are processed in passes of up to 4.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tcq {
+namespace {
+
+constexpr int kScWarps = 4;       // warps per CTA, sharing rows of one split
+constexpr int kScThreads = kScWarps * 32;
+
+template <int K, int MB>
+__global__ void __launch_bounds__(kScThreads)
+scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restrict__ codes,
+               const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+               int R, int C, int splits, int rp, int nur, float* __restrict__ partial) {
+    extern __shared__ __align__(16) float smem[];
+    float* lut_s = smem;
+    float* red = smem + kLutN;             // [kScWarps-1][MB][32 lanes][32 cols]
+    stage_lut(lut_s, lut);
+    __syncthreads();
+
+    const int s = blockIdx.x / nur;        // split
+    const int ur = blockIdx.x - s * nur;   // range of 32 units = 1024 columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = C >> 5;
+    const int unit = ur * 32 + lane;
+    const bool active = unit < units;
+    const int r0 = s * rp;
+    const int r1 = min(R, r0 + rp);
+    const int64_t wpr = (int64_t)units * K;
+    const uint32_t* tp = codes + (int64_t)unit * K;
+    const int src = next_unit_lane(lane);
+
+    float acc[MB][32];
+    #pragma unroll
+    for (int m = 0; m < MB; ++m)
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) acc[m][i] = 0.f;
+
+    uint32_t nxt[K];
+    int r = r0 + warp;
+    if (active && r < r1) load_unit<K>(nxt, tp + (int64_t)r * wpr);
+    for (; r < r1; r += kScWarps) {
+        uint32_t w[K + 1];
+        #pragma unroll
+        for (int j = 0; j < K; ++j) w[j] = nxt[j];
+        const int rn = r + kScWarps;
+        if (active && rn < r1) load_unit<K>(nxt, tp + (int64_t)rn * wpr);
+        w[K] = __shfl_sync(0xffffffffu, w[0], src);
+        const float sr = bf16_bits_to_float(__ldg(scales + r));
+        float xr[MB];
+        #pragma unroll
+        for (int m = 0; m < MB; ++m) xr[m] = bf16_bits_to_float(__ldg(x + (int64_t)(m0 + m) * R + r));
+        #pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const float v0 = lut_at(lut_s, win_off<K>(w, i));
+            const float v1 = lut_at(lut_s, win_off<K>(w, i + 1));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(v0, sr), __fmul_rn(v1, sr));
+            const float w0 = __low2float(h), w1 = __high2float(h);
+            #pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                acc[m][i] = fmaf(w0, xr[m], acc[m][i]);
+                acc[m][i + 1] = fmaf(w1, xr[m], acc[m][i + 1]);
+            }
+        }
+    }
+
+    // add the warps' partial sums (warps 1..3 stage theirs, warp 0 adds in order)
+    if (warp > 0) {
+        float* dst = red + (size_t)(warp - 1) * MB * 1024;
+        #pragma unroll
+        for (int m = 0; m < MB; ++m)
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) dst[(m * 32 + i) * 32 + lane] = acc[m][i];
+    }
+    __syncthreads();
+    if (warp == 0 && active) {
+        #pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            float v[32];
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float a = acc[m][i];
+                for (int w = 0; w < kScWarps - 1; ++w) a += red[((size_t)w * MB * 32 + m * 32 + i) * 32 + lane];
+                v[i] = a;
+            }
+            // window i <-> column c0 + 31 - i
+            const int c0 = (unit >> 3) * kBT + (224 - 32 * (unit & 7));
+            float4* dst = reinterpret_cast<float4*>(partial + ((int64_t)(m0 + m) * splits + s) * C + c0);
+            #pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(v[31 - 4 * q], v[30 - 4 * q], v[29 - 4 * q], v[28 - 4 * q]);
+        }
+    }
+}
+
+// out[m][c] = bf16( sum_s partial[m][s][c] ): a CTA covers 128 columns of one
+// activation row; 8 thread groups each add a contiguous run of splits in
+// order, and the 8 runs are then added in order.
+constexpr int kRdGroups = 8;
+
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16_t* __restrict__ out) {
+    __shared__ float4 red[kRdGroups][32];
+    const int m = blockIdx.y;
+    const int cq = blockIdx.x * 32 + (threadIdx.x & 31);   // float4 column index
+    const int grp = threadIdx.x >> 5;
+    const int per = (splits + kRdGroups - 1) / kRdGroups;
+    const int s0 = grp * per, s1 = min(splits, s0 + per);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (cq * 4 < C) {
+        const float4* p = reinterpret_cast<const float4*>(partial + (int64_t)m * splits * C) + cq;
+        const int64_t stride = C / 4;
+        for (int s = s0; s < s1; ++s) {
+            const float4 v = __ldg(p + (int64_t)s * stride);
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+    }
+    red[grp][threadIdx.x & 31] = a;
+    __syncthreads();
+    if (grp == 0 && cq * 4 < C) {
+        float4 t = red[0][threadIdx.x];
+        for (int g = 1; g < kRdGroups; ++g) {
+            const float4 v = red[g][threadIdx.x];
+            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (int64_t)m * C + cq * 4) = o;
+    }
+}
+
+template <int K, int MB>
+cudaError_t launch_pass(const Packed& p, const uint16_t* x, int m0, int splits, int rp, int nur,
+                        float* partial, cudaStream_t stream) {
+    const size_t smem = (size_t)(kLutN + (kScWarps - 1) * MB * 1024) * sizeof(float);
+    static bool configured = false;   // per template instance; benign race (idempotent)
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(scatter_kernel<K, MB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const unsigned grid = (unsigned)(splits * nur);
+    scatter_kernel<K, MB><<<grid, kScThreads, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
+                                                              (int)p.rows, (int)p.cols, splits, rp, nur, partial);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
+                     cudaStream_t stream) {
+    const int rp = (int)((p.rows + splits - 1) / splits);
+    const int units = (int)(p.cols / 32);
+    const int nur = (units + 31) / 32;
+    for (int m0 = 0; m0 < M; m0 += 4) {
+        const int mb = M - m0 < 4 ? M - m0 : 4;
+        cudaError_t e;
+        switch (mb) {
+            case 1: e = launch_pass<K, 1>(p, x, m0, splits, rp, nur, partial, stream); break;
+            case 2: e = launch_pass<K, 2>(p, x, m0, splits, rp, nur, partial, stream); break;
+            case 3: e = launch_pass<K, 3>(p, x, m0, splits, rp, nur, partial, stream); break;
+            default: e = launch_pass<K, 4>(p, x, m0, splits, rp, nur, partial, stream); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
+                           float* partial, uint16_t* out, int sm_count, cudaStream_t stream) {
+    (void)sm_count;
+    cudaError_t e;
+    switch (p.k) {
+        case 2: e = launch_k<2>(p, x, M, splits, partial, stream); break;
+        case 3: e = launch_k<3>(p, x, M, splits, partial, stream); break;
+        case 4: e = launch_k<4>(p, x, M, splits, partial, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    const int C = (int)p.cols;
+    dim3 grid((unsigned)((C / 4 + 31) / 32), (unsigned)M);
+    split_reduce_kernel<<<grid, 256, 0, stream>>>(partial, splits, C, out);
+    return cudaGetLastError();
+}
+
+}  // namespace tcq
