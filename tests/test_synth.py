@@ -46,3 +46,10 @@ def test_distributions():
     codes = synth.codes(0, 64, 1024, 4)
     bits = np.unpackbits(codes.view(np.uint8))
     assert abs(bits.mean() - 0.5) < 0.01
+
+
+def test_torch_generator_matches_numpy():
+    for seed, rows, cols, k in ((0, 3, 256, 2), (2001, 40, 1024, 3), (7, 5, 512, 4)):
+        a = synth.codes(seed, rows, cols, k)
+        b = synth.codes_torch(seed, rows, cols, k, "cpu").numpy().view(np.uint32)
+        assert np.array_equal(a, b)

@@ -1,0 +1,93 @@
+"""A synthetic stack of SwiGLU MLP layers whose weights are packed trellis codes.
+
+Per layer l (the pages only say the prefill input is the RMSNorm output; the
+SwiGLU chain is the plain reading of "Qwen's MLP geometry"):
+    n = RMSNorm(x)                  unit gain, eps 1e-6
+    g = gate(n), u = up(n)          axis 1, hidden -> intermediate
+    h = bf16(silu(g) * u)
+    x' = down(h)                    axis 0, intermediate -> hidden
+Without a residual.  Layer l, matrix j (0 gate, 1 up, 2 down) is drawn with
+seed 1000*l + j.  M = 1 uses trellis_matvec for gate/up, M >= 2 trellis_prefill;
+down always uses trellis_scatter.  Every step runs in libtrellis kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import trellis_coded_quantized_gb300 as tcq
+from . import synth
+
+HIDDEN = 5120
+INTER = 17408
+
+
+class Layer:
+    def __init__(self, l: int, k: int, device, hidden: int, inter: int):
+        import torch
+        self.mats = []
+        for j, (axis, rows, cols) in enumerate(((1, inter, hidden), (1, inter, hidden), (0, inter, hidden))):
+            seed = 1000 * l + j
+            codes = synth.codes_torch(seed, rows, cols, k, device)
+            scales = torch.from_numpy(synth.scales(seed, rows).view(np.int16)).to(device).view(torch.bfloat16)
+            lut = torch.from_numpy(synth.lut(seed)).to(device)
+            self.mats.append({"g": tcq.geometry(axis, rows, cols, k), "codes": codes,
+                              "scales": scales, "lut": lut, "seed": seed})
+
+
+class PackedMLPStack:
+    def __init__(self, layers: int = 40, k: int = 3, device="cuda", m_max: int = 16,
+                 hidden: int = HIDDEN, inter: int = INTER, splits: int = 128):
+        import torch
+        self.k, self.hidden, self.inter, self.splits = k, hidden, inter, splits
+        self.layers = [Layer(l, k, device, hidden, inter) for l in range(layers)]
+        self.device = device
+        self.m_max = m_max
+        bf = torch.bfloat16
+        self.n = torch.empty((m_max, hidden), dtype=bf, device=device)
+        self.gate = torch.empty((m_max, inter), dtype=bf, device=device)
+        self.up = torch.empty((m_max, inter), dtype=bf, device=device)
+        self.h = torch.empty((m_max, inter), dtype=bf, device=device)
+        self.xs = [torch.empty((m_max, hidden), dtype=bf, device=device) for _ in range(2)]
+        g0 = self.layers[0].mats[2]["g"]
+        self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(g0, m_max, splits) // 4,
+                              dtype=torch.float32, device=device)
+
+    @property
+    def packed_bytes(self) -> int:
+        return len(self.layers) * 3 * self.inter * self.hidden * self.k // 8
+
+    def launches_per_pass(self, M: int) -> int:
+        # rmsnorm, gate, up, silu*up, ceil(M/4) scatter passes, the split reduction
+        return len(self.layers) * (4 + (M + 3) // 4 + 1)
+
+    def layer(self, l: int, x, out, keep=None):
+        """One layer on x [M, hidden] into out [M, hidden]."""
+        M = x.shape[0]
+        gate, up, down = self.layers[l].mats
+        n, g, u, h = self.n[:M], self.gate[:M], self.up[:M], self.h[:M]
+        tcq.trellis_rmsnorm(x, 1e-6, out=n)
+        if M == 1:
+            tcq.trellis_matvec(n[0], gate["codes"], gate["scales"], gate["lut"], gate["g"], out=g[0])
+            tcq.trellis_matvec(n[0], up["codes"], up["scales"], up["lut"], up["g"], out=u[0])
+        else:
+            tcq.trellis_prefill(n, gate["codes"], gate["scales"], gate["lut"], gate["g"], out=g)
+            tcq.trellis_prefill(n, up["codes"], up["scales"], up["lut"], up["g"], out=u)
+        tcq.trellis_silu_mul(g, u, out=h)
+        tcq.trellis_scatter(h, down["codes"], down["scales"], down["lut"], down["g"], splits=self.splits,
+                            workspace=self.ws, out=out)
+        if keep is not None:
+            keep.append({"x": x.clone(), "n": n.clone(), "g": g.clone(), "u": u.clone(), "h": h.clone(),
+                         "out": out.clone()})
+        return out
+
+    def forward(self, x, layers: int | None = None, keep=None):
+        """All layers (or the first `layers`) on x [M, hidden]; returns the last output."""
+        M = x.shape[0]
+        assert 1 <= M <= self.m_max
+        cur = x
+        nl = len(self.layers) if layers is None else layers
+        for l in range(nl):
+            nxt = self.xs[l % 2][:M]
+            self.layer(l, cur, nxt, keep)
+            cur = nxt
+        return cur

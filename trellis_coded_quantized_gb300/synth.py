@@ -115,3 +115,41 @@ def problem(axis: int, m: int, rows: int, cols: int, k: int, seed: int = 0) -> d
         "lut": lut(seed),
         "x": activations(seed, m, kin),
     }
+
+
+# ----------------------------------------------------------------------------
+# the same codes drawn on a torch device (for multi-GB inputs)
+# ----------------------------------------------------------------------------
+
+def _s64(v: int) -> int:
+    """A 64-bit pattern as a signed int64 constant."""
+    v &= 0xFFFFFFFFFFFFFFFF
+    return v - (1 << 64) if v >= (1 << 63) else v
+
+
+def _mix_t(z):
+    import torch
+    z = z ^ ((z >> 30) & ((1 << 34) - 1))
+    z = z * _s64(_M1)
+    z = z ^ ((z >> 27) & ((1 << 37) - 1))
+    z = z * _s64(_M2)
+    z = z ^ ((z >> 31) & ((1 << 33) - 1))
+    return z
+
+
+def codes_torch(seed: int, rows: int, cols: int, k: int, device, bt: int = BT):
+    """``codes(seed, rows, cols, k)`` computed with int64 tensor arithmetic
+    (wrapping multiply, masked logical shifts) on ``device``; int32 storage."""
+    import torch
+    w = words_per_row(cols, k, bt)
+    n = rows * w
+    s = np.array([(int(seed) ^ (TAG_CODES * _TAG)) & 0xFFFFFFFFFFFFFFFF], np.uint64)
+    base = _s64(int(_mix(s)[0]))
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    chunk = 1 << 24
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        i = torch.arange(lo + 1, hi + 1, dtype=torch.int64, device=device)
+        z = _mix_t(i * _s64(GAMMA) + base)
+        out[lo:hi] = ((z >> 32) & 0xFFFFFFFF).to(torch.int32)
+    return out.view(rows, w)
