@@ -118,6 +118,28 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
                                float* workspace, size_t workspace_bytes,
                                void* out, void* stream);
 
+/*
+ * trellis_scatter without a caller-provided workspace.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory,
+ * such as plugin interfaces that pass in only input and output buffers, or
+ * serving loops that must not call cudaMalloc because it can synchronise the
+ * device.  Same arguments and result as trellis_scatter minus the workspace;
+ * the fp32 split partials go to a 16 MiB array of device memory that the
+ * library declares itself (reserved on every GPU that loads the library
+ * until the process exits).
+ *   - M * splits * cols must be at most 4,194,304 (splits 0 means 128),
+ *     else TRELLIS_ERR_WORKSPACE and nothing is enqueued;
+ *   - allocates nothing; the first call on a device looks up the array's
+ *     device address (cudaGetSymbolAddress), so make that first call before
+ *     any stream capture;
+ *   - all calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ */
+trellis_status trellis_scatter_noalloc(const void* x, int32_t M, const uint32_t* codes,
+                                       const void* scales, const float* lut,
+                                       const trellis_geometry* g, int32_t splits,
+                                       void* out, void* stream);
+
 /* M * splits * cols * 4 bytes (splits 0 means 128); 0 for invalid arguments. */
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits);
 

@@ -139,6 +139,21 @@ def trellis_scatter(x, codes, scales, lut, g, splits: int = 0, workspace=None, o
     return out
 
 
+def trellis_scatter_noalloc(x, codes, scales, lut, g, splits: int = 0, out=None, stream=None):
+    """Axis 0 like trellis_scatter, for callers that cannot allocate device
+    memory: the split partials live in the library's own 16 MiB device array,
+    so M * splits * cols may be at most 4,194,304.  Allocates nothing when
+    `out` is given.  Calls that overlap on the GPU share that array and race."""
+    c, s, t = _packed(codes, scales, lut, g)
+    M = x.shape[0]
+    xp = _dev(x, "x", _bf16_types(), (M, g.rows))
+    out = _out(out, (M, g.cols), x)
+    op = _dev(out, "out", _bf16_types(), (M, g.cols))
+    _check(_lib.load().trellis_scatter_noalloc(xp, M, c, s, t, ctypes.byref(g), splits, op, _stream(stream)),
+           "trellis_scatter_noalloc")
+    return out
+
+
 def trellis_expand(codes, scales, lut, g, w_out=None, win_out=None, with_windows=False, stream=None):
     """Decode the packed matrix: w bf16 [rows, cols] (and windows int16 [rows, cols])."""
     torch = _torch()

@@ -11,7 +11,8 @@ LIB_PATH = os.path.join(HERE, "libtrellis.so")
 
 # the entry points declared in include/trellis.h
 EXPORTS = (
-    "trellis_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_workspace_bytes",
+    "trellis_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_noalloc",
+    "trellis_scatter_workspace_bytes",
     "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_gather_probe",
     "trellis_device_status", "trellis_strerror",
 )
@@ -47,6 +48,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "trellis_matvec": ([P, P, P, P, G, P, P], I32),
             "trellis_prefill": ([P, I32, P, P, P, G, P, P], I32),
             "trellis_scatter": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
+            "trellis_scatter_noalloc": ([P, I32, P, P, P, G, I32, P, P], I32),
             "trellis_scatter_workspace_bytes": ([G, I32, I32], SZ),
             "trellis_expand": ([P, P, P, G, P, P, P], I32),
             "trellis_rmsnorm": ([P, I64, I64, ctypes.c_float, P, P], I32),

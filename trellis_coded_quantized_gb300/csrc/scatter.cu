@@ -208,3 +208,58 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
 }
 
 }  // namespace tcq
+
+// ---------------------------------------------------------------------------
+// trellis_scatter_noalloc: trellis_scatter with library-owned scratch.
+//
+// Some callers cannot hand the scatter a workspace: for example a plugin
+// interface of an inference runtime that passes in only the input and output
+// buffers, or a serving loop that must not call cudaMalloc because it can
+// synchronise the device and stall every other stream.  This entry point
+// keeps the fp32 split partials in a fixed array in device memory that the
+// library itself declares, so the call needs no allocation at all.  The
+// array is created when the library is loaded onto a GPU and stays reserved
+// on every GPU that loads the library until the process exits.
+// ---------------------------------------------------------------------------
+#include "trellis.h"
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;   // 16 MiB
+static __device__ __align__(256) float g_scatter_scratch[kNoAllocScratchFloats];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::once_flag g_scratch_once[kNoAllocMaxDevices];
+float* g_scratch_ptr[kNoAllocMaxDevices];
+cudaError_t g_scratch_err[kNoAllocMaxDevices];
+
+}  // namespace
+
+extern "C" trellis_status trellis_scatter_noalloc(const void* x, int32_t M, const uint32_t* codes,
+                                                  const void* scales, const float* lut,
+                                                  const trellis_geometry* g, int32_t splits,
+                                                  void* out, void* stream) {
+    if (!g) return TRELLIS_ERR_NULL;
+    const size_t need = trellis_scatter_workspace_bytes(g, M, splits);
+    if (need > kNoAllocScratchFloats * sizeof(float)) return TRELLIS_ERR_WORKSPACE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return TRELLIS_ERR_DEVICE;
+    }
+    // Once per device, with that device current: the device address of the
+    // scratch array (its name in host code is only a host-side stand-in).
+    std::call_once(g_scratch_once[dev], [dev]() {
+        void* p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_scatter_scratch);
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+        if (g_scratch_err[dev] != cudaSuccess) cudaGetLastError();
+    });
+    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return TRELLIS_ERR_DEVICE;
+    // Every partial the reduction reads is written by this same call (empty
+    // splits store zeros), so nothing in the scratch has to be cleared first.
+    return trellis_scatter(x, M, codes, scales, lut, g, splits, g_scratch_ptr[dev],
+                           kNoAllocScratchFloats * sizeof(float), out, stream);
+}
