@@ -34,9 +34,6 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-M1, K1, N1, KB1 = 1, 5120, 17408, 4          # the decode-matvec workload
-PACKED_BYTES = N1 * K1 * KB1 // 8             # 44,564,480
-WORKLOAD = "decode matvec axis-1: M=1, K=5120, N=17408, k=4, BT=256, L=12"
 METRIC = "packed-weight GB/s & % HBM roofline (M=1); TFLOP/s & % roofline (M=5..32)"
 
 
@@ -53,24 +50,39 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def profiled_traffic(kernel_file: str):
-    """dram bytes per launch from profiles/<...>.md when it was captured on the
-    current source of the kernel (the summary records the source's sha1)."""
+def source_fingerprint(kernel_file: str):
+    """sha1 (12 hex digits) of a kernel source with comments and blank lines
+    removed, so that editing documentation does not void a capture."""
     src = os.path.join(ROOT, "trellis_coded_quantized_gb300", "csrc", kernel_file)
     try:
-        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        text = open(src).read()
     except OSError:
+        return None
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    code = "\n".join(ln for ln in lines if ln.strip())
+    return hashlib.sha1(code.encode()).hexdigest()[:12]
+
+
+def profiled_traffic(kernel_file: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from a summary under profiles/ when it
+    was captured on the current source of the kernel (the summary records the
+    source's fingerprint): a line "traffic_per_launch_bytes: B source_sha1: S
+    kernel_file: F kernel: K"."""
+    sha = source_fingerprint(kernel_file)
+    if sha is None:
         return None
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
+    pat = re.compile(r"traffic_per_launch_bytes:\s*(\d+)\s+source_sha1:\s*([0-9a-f]+)\s+"
+                     r"kernel_file:\s*(\S+)\s+kernel:\s*(.+)$", re.M)
     for name in sorted(os.listdir(pdir)):
         if not name.endswith(".md"):
             continue
-        text = open(os.path.join(pdir, name)).read()
-        m = re.search(r"traffic_per_launch_bytes:\s*(\d+)\s+source_sha1:\s*([0-9a-f]+)\s+kernel_file:\s*(\S+)", text)
-        if m and m.group(3) == kernel_file and m.group(2) == sha:
-            return int(m.group(1))
+        for m in pat.finditer(open(os.path.join(pdir, name)).read()):
+            if m.group(3) == kernel_file and m.group(2) == sha and m.group(4).strip() == kernel:
+                return int(m.group(1))
     return None
 
 
@@ -134,17 +146,84 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
-def make_sets(torch, tcq, nsets: int, device):
-    from trellis_coded_quantized_gb300 import synth
-    p = synth.problem(1, M1, N1, K1, KB1, seed=0)
-    codes0 = torch.from_numpy(p["codes"].view(np.int32)).to(device)
-    scales = torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16)
-    lut = torch.from_numpy(p["lut"]).to(device)
-    x = torch.from_numpy(p["x"].view(np.int16)).to(device).view(torch.bfloat16)[0]
-    # further weight sets: the first XOR a per-set constant (still uniform codes)
-    sets = [codes0] + [codes0 ^ int(np.int32(np.uint32((0x9E3779B9 * (j + 1)) & 0xFFFFFFFF)))
+def xor_sets(torch, codes0, nsets: int, salt: int):
+    """Further weight sets for L2 rotation: the first XOR a per-set constant
+    (uniform codes stay uniform)."""
+    return [codes0] + [codes0 ^ int(np.int32(np.uint32((salt * (j + 1)) & 0xFFFFFFFF)))
                        for j in range(1, nsets)]
-    return p, sets, scales, lut, x
+
+
+def dev_problem(torch, p, device):
+    return (torch.from_numpy(p["codes"].view(np.int32)).to(device),
+            torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16),
+            torch.from_numpy(p["lut"]).to(device),
+            torch.from_numpy(p["x"].view(np.int16)).to(device).view(torch.bfloat16))
+
+
+class Workload:
+    """One configuration: step(i) runs one pass of the hot path on weight set
+    i mod nsets; the step's launches are timed for the roofline."""
+
+    def __init__(self, args, torch, tcq, device, l2):
+        from trellis_coded_quantized_gb300 import synth
+        self.args, self.torch, self.tcq, self.device = args, torch, tcq, device
+        w = args.workload
+        self.name = w
+        if w in ("decode-matvec", "tiny-matvec"):
+            M, K, N, k = (1, 5120, 17408, 4) if w == "decode-matvec" else (1, 512, 256, 2)
+            self.M, self.K, self.N, self.k, self.axis = M, K, N, k, 1
+            self.desc = (f"decode matvec axis-1: M=1, K={K}, N={N}, k={k}, BT=256, L=12" if w == "decode-matvec"
+                         else f"tiny axis-1 matvec: M=1, K={K}, N={N}, k={k}, BT=256, L=12, seed 0")
+            self.kernel = f"matvec_kernel<{k}>"
+            self.kernel_file = "matvec.cu"
+        elif w == "prefill":
+            self.M, self.K, self.N, self.k, self.axis = args.M or 32, 5120, 17408, args.k or 4, 1
+            self.desc = f"tiled prefill axis-1: M={self.M}, K=5120, N=17408, k={self.k}, BT=256, L=12"
+            self.kernel = f"prefill_kernel<{self.k},{16 if self.M <= 16 else 32}>"
+            self.kernel_file = "prefill.cu"
+        elif w == "scatter":
+            self.M, self.K, self.N, self.k, self.axis = args.M or 1, 17408, 5120, 3, 0
+            self.desc = f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, 128 splits"
+            self.kernel = "scatter_kernel<3> + split_reduce_kernel"
+            self.kernel_file = "scatter.cu"
+        else:
+            raise ValueError(w)
+        rows, cols = (self.N, self.K) if self.axis == 1 else (self.K, self.N)
+        self.rows, self.cols = rows, cols
+        self.packed = rows * cols * self.k // 8
+        self.flops = 2.0 * self.M * rows * cols
+        p = synth.problem(self.axis, self.M, rows, cols, self.k, seed=0)
+        self.p = p
+        codes0, self.scales, self.lut, self.x = dev_problem(torch, p, device)
+        self.nsets = max(2, int(np.ceil(4 * l2 / self.packed)) + 1)
+        self.sets = xor_sets(torch, codes0, self.nsets, 0x9E3779B9)
+        self.g = tcq.geometry(self.axis, rows, cols, self.k)
+        nout = rows if self.axis == 1 else cols
+        self.out = torch.empty((self.M, nout), dtype=torch.bfloat16, device=device)
+        self.ws = None
+        if w == "scatter":
+            self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(self.g, self.M, 128) // 4,
+                                  dtype=torch.float32, device=device)
+        # algorithmic bytes of the dominant launch: codes, scales, codebook, x, out
+        self.alg_bytes = self.packed + rows * 2 + 4096 * 4 + self.M * (cols if self.axis == 1 else rows) * 2 \
+            + self.M * nout * 2
+        if w == "scatter":   # the split partials are written and read back once
+            self.alg_bytes += 2 * self.M * 128 * cols * 4
+        self.launches_per_step = 1 if w != "scatter" else 1 + (self.M + 3) // 4
+
+    def run(self, codes, x=None, out=None):
+        tcq = self.tcq
+        x = self.x if x is None else x
+        out = self.out if out is None else out
+        if self.name in ("decode-matvec", "tiny-matvec"):
+            tcq.trellis_matvec(x[0], codes, self.scales, self.lut, self.g, out=out[0])
+        elif self.name == "prefill":
+            tcq.trellis_prefill(x, codes, self.scales, self.lut, self.g, out=out)
+        else:
+            tcq.trellis_scatter(x, codes, self.scales, self.lut, self.g, splits=128, workspace=self.ws, out=out)
+
+    def step(self, i):
+        self.run(self.sets[i % self.nsets])
 
 
 def time_launches(torch, fn, steps, warmup, stream, barrier):
@@ -170,61 +249,56 @@ def time_launches(torch, fn, steps, warmup, stream, barrier):
     return total_ms, per
 
 
-def extra_configs(torch, tcq, device, stream, peaks):
-    """Throughput of the other configurations (secondary figures)."""
-    from trellis_coded_quantized_gb300 import synth
+def secondary(torch, tcq, device, stream, peaks, l2):
+    """Median launch times of the other configurations (context figures)."""
     out = {}
     hbm = peaks["hbm_gbs"]
     tc_peak = peaks["bf16_tflops"]
-    reps = 30
-    # prefill M x k (axis 1, K=5120, N=17408)
-    for k in (2, 3, 4):
-        p = synth.problem(1, 32, N1, K1, k, seed=0)
-        codes = [torch.from_numpy(p["codes"].view(np.int32)).to(device)]
-        codes += [codes[0] ^ int(np.int32(np.uint32((0x85EBCA6B * (j + 1)) & 0xFFFFFFFF))) for j in range(1, 8)]
-        sc = torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16)
-        lut = torch.from_numpy(p["lut"]).to(device)
-        g = tcq.geometry(1, N1, K1, k)
-        packed = N1 * K1 * k // 8
-        for M in (5, 8, 16, 32):
-            x = torch.from_numpy(p["x"][:M].view(np.int16)).to(device).view(torch.bfloat16)
-            o = torch.empty((M, N1), dtype=torch.bfloat16, device=device)
-            fn = lambda i: tcq.trellis_prefill(x, codes[i % len(codes)], sc, lut, g, out=o)
-            _, per = time_launches(torch, fn, reps, 3, stream, lambda: None)
-            t = statistics.median(per) * 1e-3
-            flops = 2.0 * M * N1 * K1
-            roof = min(hbm * 1e9 * flops / packed, tc_peak * 1e12)
-            out[f"prefill_M{M}_k{k}"] = {
-                "us": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
-                "packed_gbs": round(packed / t / 1e9, 1), "tokens_per_s": round(M / t, 1),
-                "frac_of_roofline": round(flops / t / roof, 4)}
-    # scatter (axis 0, R=17408, C=5120, k=3, 128 splits)
-    p = synth.problem(0, 4, N1, K1, 3, seed=0)
-    codes = [torch.from_numpy(p["codes"].view(np.int32)).to(device)]
-    codes += [codes[0] ^ int(np.int32(np.uint32((0xC2B2AE35 * (j + 1)) & 0xFFFFFFFF))) for j in range(1, 8)]
-    sc = torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16)
-    lut = torch.from_numpy(p["lut"]).to(device)
-    g = tcq.geometry(0, N1, K1, 3)
-    packed = N1 * K1 * 3 // 8
-    for M in (1, 4):
-        x = torch.from_numpy(p["x"][:M].view(np.int16)).to(device).view(torch.bfloat16)
-        ws = torch.empty(tcq.trellis_scatter_workspace_bytes(g, M, 128) // 4, dtype=torch.float32, device=device)
-        o = torch.empty((M, K1), dtype=torch.bfloat16, device=device)
-        fn = lambda i: tcq.trellis_scatter(x, codes[i % len(codes)], sc, lut, g, splits=128, workspace=ws, out=o)
-        _, per = time_launches(torch, fn, reps, 3, stream, lambda: None)
+
+    class A:
+        pass
+    for w, M, k in ([("prefill", M, k) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
+                    [("scatter", 1, 3), ("scatter", 4, 3), ("tiny-matvec", 1, 2)]):
+        a = A()
+        a.workload, a.M, a.k = w, M, k
+        wl = Workload(a, torch, tcq, device, l2)
+        _, per = time_launches(torch, wl.step, 30, 3, stream, lambda: None)
         t = statistics.median(per) * 1e-3
-        out[f"scatter_M{M}_k3_s128"] = {"us": round(t * 1e6, 2), "packed_gbs": round(packed / t / 1e9, 1),
-                                        "frac_of_hbm": round(packed / t / 1e9 / hbm, 4),
-                                        "tokens_per_s": round(M / t, 1)}
-    # shared-memory gather rate (the decode's other roofline)
+        key = f"{w}_M{M}_k{k}"
+        rec = {"us": round(t * 1e6, 2), "packed_gbs": round(wl.packed / t / 1e9, 1),
+               "tokens_per_s": round(M / t, 1), "frac_of_hbm_alg": round(wl.alg_bytes / t / 1e9 / hbm, 4)}
+        if w == "prefill":
+            roof = min(hbm * 1e9 * wl.flops / wl.packed, tc_peak * 1e12)
+            rec["tflops"] = round(wl.flops / t / 1e12, 2)
+            rec["frac_of_roofline"] = round(wl.flops / t / roof, 4)
+        out[key] = rec
+        del wl
+        torch.cuda.empty_cache()
+    # the 40-layer MLP stack, M = 1 and 16
+    from trellis_coded_quantized_gb300.mlp import PackedMLPStack
+    stack = PackedMLPStack(layers=40, k=3, device=device, m_max=16)
+    from trellis_coded_quantized_gb300 import synth
+    for M in (1, 16):
+        x0 = torch.from_numpy(synth.activations(0, M, 5120).view(np.int16)).to(device).view(torch.bfloat16)
+        _, per = time_launches(torch, lambda i: stack.forward(x0), 5, 2, stream, lambda: None)
+        t = statistics.median(per) * 1e-3
+        out[f"mlp40_M{M}_k3"] = {"ms_per_pass": round(t * 1e3, 3), "tokens_per_s": round(M / t, 1),
+                                 "packed_gbs": round(stack.packed_bytes / t / 1e9, 1),
+                                 "tflops": round(2.0 * M * stack.packed_bytes * 8 / 3 / t / 1e12, 2),
+                                 "launches_per_pass": stack.launches_per_pass(M)}
+    del stack
+    torch.cuda.empty_cache()
+    # shared-memory gather rate (the decode's second roofline), with 1, 4 and 8 table copies
     lut = torch.randn(4096, device=device)
     sm = torch.cuda.get_device_properties(device).multi_processor_count
     iters = 2000
-    fn = lambda i: tcq.trellis_gather_probe(lut, sm, iters)
-    _, per = time_launches(torch, fn, 5, 2, stream, lambda: None)
-    t = statistics.median(per) * 1e-3
-    gathers = sm * 1024 * iters * 8
-    out["smem_gather"] = {"gathers_per_s": gathers / t, "per_sm_per_clock_at_max": gathers / t / sm / 2.07e9}
+    for rep in (1, 4, 8):
+        _, per = time_launches(torch, lambda i: tcq.trellis_gather_probe(lut, sm, iters, rep), 5, 2,
+                               stream, lambda: None)
+        t = statistics.median(per) * 1e-3
+        gathers = sm * 1024 * iters * 8
+        out[f"smem_gather_x{rep}"] = {"gathers_per_s": gathers / t,
+                                      "per_sm_per_clock_at_2070MHz": round(gathers / t / sm / 2.07e9, 3)}
     return out
 
 
@@ -241,88 +315,89 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     barrier = (lambda: dist.barrier()) if dist else (lambda: None)
     peaks, peak_src = measured_peaks()
-
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    nsets = max(4, int(np.ceil(4 * l2 / PACKED_BYTES)) + 1)
-    p, sets, scales, lut, x = make_sets(torch, tcq, nsets, device)
-    g = tcq.geometry(1, N1, K1, KB1)
-    out = torch.empty(N1, dtype=torch.bfloat16, device=device)
 
-    def step(i):
-        tcq.trellis_matvec(x, sets[i % nsets], scales, lut, g, out=out)
-
+    wl = Workload(args, torch, tcq, device, l2)
     with ClockSampler(local_rank) as clk:
-        total_ms, per = time_launches(torch, step, args.steps, args.warmup, stream, barrier)
-    ms = total_ms / args.steps
+        total_ms, per = time_launches(torch, wl.step, args.steps, args.warmup, stream, barrier)
     if dist:
         t = torch.tensor([total_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-        ms = total_ms / args.steps
-    value = world * PACKED_BYTES * args.steps / (total_ms * 1e-3) / 1e9
+    ms = total_ms / args.steps
+    sec = total_ms * 1e-3
+    if wl.name == "prefill":
+        value, unit = world * wl.flops * args.steps / sec / 1e12, "TFLOP/s"
+    else:
+        value, unit = world * wl.packed * args.steps / sec / 1e9, "GB/s"
 
-    # roofline of the dominant kernel (the matvec: the only kernel of the step)
+    # roofline of the dominant launch (the only launch of the step, or the
+    # scatter with its split reduction)
     kern_s = statistics.mean(per) * 1e-3
-    alg_bytes = PACKED_BYTES + N1 * 2 + K1 * 2 + N1 * 2 + 4096 * 4
-    achieved = alg_bytes / kern_s / 1e9
+    achieved = wl.alg_bytes / kern_s / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": profiled_traffic("matvec.cu"), "kernel": "matvec_kernel<4>",
-                "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                "kernel_us": round(kern_s * 1e6, 3)}
+                "traffic": profiled_traffic(wl.kernel_file, wl.kernel), "kernel": wl.kernel,
+                "peak_source": f"{peak_src} hbm_gbs (burst copy)", "kernel_us": round(kern_s * 1e6, 3),
+                "algorithmic_bytes": wl.alg_bytes}
 
-    # end to end: pinned host inputs -> device, matvec through the C ABI, result -> host
-    e2e = None
-    if rank == 0 or world > 1:
-        h_codes = torch.from_numpy(p["codes"].view(np.int32)).pin_memory()
-        h_scales = torch.from_numpy(p["scales"].view(np.int16)).pin_memory()
-        h_lut = torch.from_numpy(p["lut"]).pin_memory()
-        h_x = torch.from_numpy(p["x"][0].view(np.int16)).pin_memory()
-        h_out = torch.empty(N1, dtype=torch.int16).pin_memory()
-        d_codes = torch.empty_like(sets[0])
-        d_scales = torch.empty(N1, dtype=torch.int16, device=device)
-        d_lut = torch.empty(4096, dtype=torch.float32, device=device)
-        d_x = torch.empty(K1, dtype=torch.int16, device=device)
-        d_out = torch.empty(N1, dtype=torch.int16, device=device)
+    # end to end: pinned host inputs -> device, the C-ABI call, result -> host
+    h = {"codes": torch.from_numpy(wl.p["codes"].view(np.int32)).pin_memory(),
+         "scales": torch.from_numpy(wl.p["scales"].view(np.int16)).pin_memory(),
+         "lut": torch.from_numpy(wl.p["lut"]).pin_memory(),
+         "x": torch.from_numpy(wl.p["x"].view(np.int16)).pin_memory()}
+    h_out = torch.empty(tuple(wl.out.shape), dtype=torch.int16).pin_memory()
+    d = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h.items()}
+    d_out = torch.empty(tuple(wl.out.shape), dtype=torch.int16, device=device)
 
-        def e2e_step(i):
-            d_codes.copy_(h_codes, non_blocking=True)
-            d_scales.copy_(h_scales, non_blocking=True)
-            d_lut.copy_(h_lut, non_blocking=True)
-            d_x.copy_(h_x, non_blocking=True)
-            tcq.trellis_matvec(d_x, d_codes, d_scales, d_lut, g, out=d_out)
-            h_out.copy_(d_out, non_blocking=True)
+    def e2e_step(i):
+        for k in d:
+            d[k].copy_(h[k], non_blocking=True)
+        sc, lt = wl.scales, wl.lut
+        wl.scales, wl.lut = d["scales"].view(torch.bfloat16), d["lut"]
+        wl.run(d["codes"], x=d["x"].view(torch.bfloat16), out=d_out.view(torch.bfloat16))
+        wl.scales, wl.lut = sc, lt
+        h_out.copy_(d_out, non_blocking=True)
 
-        e_steps = max(10, min(200, args.steps // 20))
-        e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier)
-        bi = PACKED_BYTES + N1 * 2 + 4096 * 4 + K1 * 2
-        bo = N1 * 2
-        e2e = {"value": round(world * PACKED_BYTES * e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": round(e_ms / e_steps, 4)}
+    e_steps = max(10, min(200, args.steps // 20))
+    e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier)
+    if dist:
+        t = torch.tensor([e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    bi = sum(v.numel() * v.element_size() for v in h.values())
+    bo = h_out.numel() * 2
+    work = wl.flops / 1e12 if wl.name == "prefill" else wl.packed / 1e9
+    e2e = {"value": round(world * work * e_steps / (e_ms * 1e-3), 3), "unit": unit,
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e_ms / e_steps, 4)}
 
     extras = None
     if rank == 0 and not args.no_extras:
-        extras = extra_configs(torch, tcq, device, stream, peaks)
+        del wl.sets
+        torch.cuda.empty_cache()
+        extras = secondary(torch, tcq, device, stream, peaks, l2)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(seconds=args.cpu_seconds)
+        cpu = cpu_baseline(wl, seconds=args.cpu_seconds)
 
+    torch.cuda.synchronize()
     status = tcq.trellis_device_status()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded SplitMix64 codes, N(0,1) codebook and activations, U[0.01,0.03] scales)",
-            "config": {"workload": WORKLOAD, "M": M1, "K": K1, "N": N1, "k": KB1, "BT": 256, "L": 12,
-                       "weight_sets": nsets, "l2": f"inputs larger than L2: {nsets} rotating weight sets "
-                                                   f"({nsets * PACKED_BYTES / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+            "config": {"workload": wl.desc, "M": wl.M, "K_in": wl.cols if wl.axis == 1 else wl.rows,
+                       "N_out": wl.rows if wl.axis == 1 else wl.cols, "k": wl.k, "BT": 256, "L": 12,
+                       "axis": wl.axis, "weight_sets": wl.nsets,
+                       "l2": f"inputs larger than L2: {wl.nsets} rotating weight sets "
+                             f"({wl.nsets * wl.packed / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clk.summary(), "device_status": status,
-            "secondary": extras,
+            "gpu_launches": args.steps * wl.launches_per_step, "clocks": clk.summary(),
+            "device_status": status, "secondary": extras,
         }
         print(json.dumps(line))
     if dist:
@@ -333,32 +408,61 @@ def run_ours(args):
 # the oracle as the CPU baseline / reference arm
 # ---------------------------------------------------------------------------
 
-def oracle_rows_per_second(orc, p, rows):
-    """Decode + double matvec of `rows` rows of the decode-matvec problem."""
+def oracle_pass(orc, wl, rows):
+    """The oracle on the first `rows` rows of the workload's packed matrix:
+    expand them to bf16 weights, then the double contraction (axis 1: those
+    output rows; axis 0: the sum over those input rows)."""
+    p = wl.p
     codes = p["codes"][:rows]
     t0 = time.perf_counter()
-    W, _ = orc.expand(codes, rows, K1, KB1, p["scales"][:rows], p["lut"])
-    orc.matmul_axis1(p["x"], W)
-    return rows / (time.perf_counter() - t0)
+    W, _ = orc.expand(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
+    if wl.axis == 1:
+        orc.matmul_axis1(p["x"], W)
+    else:
+        orc.matmul_axis0(p["x"][:, :rows], W)
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(seconds: float = 10.0, p=None):
+def cpu_baseline(wl, seconds: float = 10.0):
     import oracle
-    from trellis_coded_quantized_gb300 import synth
     orc = oracle.default()
-    if p is None:
-        p = synth.problem(1, M1, N1, K1, KB1, seed=0)
-    rps = oracle_rows_per_second(orc, p, 512)
-    rows = int(min(N1, max(512, rps * 1.0)))
+    t = oracle_pass(orc, wl, min(wl.rows, 256))
+    rows = int(min(wl.rows, max(16, 256 * 1.0 / max(t, 1e-6))))   # about a second per pass
     done_rows, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds:
-        oracle_rows_per_second(orc, p, rows)
+        oracle_pass(orc, wl, rows)
         done_rows += rows
     el = time.perf_counter() - t0
-    value = done_rows * K1 * KB1 / 8 / el / 1e9
-    return {"value": round(value, 4), "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
-            "sample": f"{done_rows} rows of the decode-matvec matrix ({rows} per pass: expand to bf16 "
-                      f"weights + double matvec), {el:.1f} s"}
+    frac = done_rows / wl.rows
+    if wl.name == "prefill":
+        value, unit = frac * wl.flops / el / 1e12, "TFLOP/s"
+    else:
+        value, unit = frac * wl.packed / el / 1e9, "GB/s"
+    return {"value": round(value, 6), "unit": unit, "cores": orc.max_threads(), "kind": "oracle",
+            "sample": f"{done_rows} of the {wl.rows} matrix rows ({rows} per pass: expand to bf16 weights "
+                      f"+ double contraction), {el:.1f} s"}
+
+
+class _HostWorkload:
+    """The workload's sizes and seeded inputs without a GPU (reference arm)."""
+
+    def __init__(self, args):
+        from trellis_coded_quantized_gb300 import synth
+        w = args.workload
+        self.name = w
+        if w == "decode-matvec":
+            self.M, rows, cols, self.k, self.axis = 1, 17408, 5120, 4, 1
+        elif w == "tiny-matvec":
+            self.M, rows, cols, self.k, self.axis = 1, 256, 512, 2, 1
+        elif w == "prefill":
+            self.M, rows, cols, self.k, self.axis = args.M or 32, 17408, 5120, args.k or 4, 1
+        else:
+            self.M, rows, cols, self.k, self.axis = args.M or 1, 17408, 5120, 3, 0
+        self.rows, self.cols = rows, cols
+        self.packed = rows * cols * self.k // 8
+        self.flops = 2.0 * self.M * rows * cols
+        self.p = synth.problem(self.axis, self.M, rows, cols, self.k, seed=0)
+        self.desc = f"{w}: M={self.M}, rows={rows}, cols={cols}, k={self.k}, axis {self.axis}"
 
 
 def run_reference(args):
@@ -366,29 +470,32 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    from trellis_coded_quantized_gb300 import synth
     orc = oracle.default()
-    p = synth.problem(1, M1, N1, K1, KB1, seed=0)
-    rps = oracle_rows_per_second(orc, p, 512)
+    wl = _HostWorkload(args)
+    t = oracle_pass(orc, wl, min(wl.rows, 256))
     budget = 60.0
-    rows = int(max(8, min(N1, budget * rps / max(1, args.steps + args.warmup))))
+    per_row = t / min(wl.rows, 256)
+    rows = int(max(8, min(wl.rows, budget / per_row / max(1, args.steps + args.warmup))))
     for _ in range(args.warmup):
-        oracle_rows_per_second(orc, p, rows)
+        oracle_pass(orc, wl, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_rows_per_second(orc, p, rows)
+        oracle_pass(orc, wl, rows)
     el = time.perf_counter() - t0
-    value = rows * K1 * KB1 / 8 * args.steps / el / 1e9
+    frac = rows / wl.rows * args.steps
+    if wl.name == "prefill":
+        value, unit = frac * wl.flops / el / 1e12, "TFLOP/s"
+    else:
+        value, unit = frac * wl.packed / el / 1e9, "GB/s"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (same seeded inputs)",
-        "config": {"workload": WORKLOAD, "M": M1, "K": K1, "N": N1, "k": KB1,
-                   "sample": f"{rows} of {N1} rows per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
-                         "sample": f"{rows} rows of the decode-matvec matrix per step"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "data": "synthetic (the same seeded inputs)",
+        "config": {"workload": wl.desc, "sample": f"{rows} of {wl.rows} rows per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": orc.max_threads(), "kind": "oracle",
+                         "sample": f"{rows} of the {wl.rows} matrix rows per step (expand + double contraction)"},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
@@ -396,10 +503,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--workload", choices=["decode-matvec", "tiny-matvec", "prefill", "scatter"],
+                    default="decode-matvec")
+    ap.add_argument("--M", type=int, default=0, help="activation rows (prefill: 32, scatter: 1)")
+    ap.add_argument("--k", type=int, default=0, help="bits per symbol of the prefill (4)")
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

@@ -168,13 +168,15 @@ trellis_status trellis_silu_mul(const void* g, const void* u, int64_t n,
                                 void* out, void* stream);
 
 /*
- * Measurement aid: time-free kernel that performs `iters` rounds of random
- * 4-byte gathers from a 4096-entry f32 table held in shared memory, on
- * `blocks` CTAs of 1024 threads, and writes one float per thread to sink
- * (f32 [blocks*1024]) so that nothing is optimised away.  Timing it with
- * events gives the shared-memory gather rate that bounds the decode.
+ * Measurement aid: `iters` rounds of 8 random 4-byte gathers per thread from
+ * a 4096-entry f32 table held in shared memory, on `blocks` CTAs of 1024
+ * threads; one float per thread goes to sink (f32 [blocks*1024]) so nothing
+ * is optimised away.  Timed with events it gives the shared-memory gather
+ * rate that bounds the decode.  replicas 1: one table; 4 or 8: copies of the
+ * table interleaved so that lane group lane % replicas reads only its own
+ * banks (entry e of copy g at word replicas*e + g).
  */
-trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t iters,
+trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t iters, int32_t replicas,
                                     float* sink, void* stream);
 
 /*

@@ -116,5 +116,6 @@ def test_glue_validation(lib):
     assert lib.trellis_rmsnorm(None, 1, 16, ctypes.c_float(1e-6), _p(A), None) == NULL
     assert lib.trellis_rmsnorm(_p(A), 1, 70000, ctypes.c_float(1e-6), _p(A), None) == SHAPE
     assert lib.trellis_silu_mul(_p(A), _p(A), 0, _p(A), None) == SHAPE
-    assert lib.trellis_gather_probe(_p(A), 0, 1, _p(A), None) == SHAPE
-    assert lib.trellis_gather_probe(_p(U), 1, 1, _p(A), None) == ALIGN
+    assert lib.trellis_gather_probe(_p(A), 0, 1, 1, _p(A), None) == SHAPE
+    assert lib.trellis_gather_probe(_p(A), 1, 1, 3, _p(A), None) == SHAPE
+    assert lib.trellis_gather_probe(_p(U), 1, 1, 1, _p(A), None) == ALIGN

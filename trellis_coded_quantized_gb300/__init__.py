@@ -186,13 +186,14 @@ def trellis_silu_mul(g_, u, out=None, stream=None):
     return out
 
 
-def trellis_gather_probe(lut, blocks: int, iters: int, sink=None, stream=None):
+def trellis_gather_probe(lut, blocks: int, iters: int, replicas: int = 1, sink=None, stream=None):
     torch = _torch()
     lp = _dev(lut, "lut", (torch.float32,), (1 << L,))
     if sink is None:
         sink = torch.empty(blocks * 1024, dtype=torch.float32, device=lut.device)
     sp = _dev(sink, "sink", (torch.float32,), (blocks * 1024,))
-    _check(_lib.load().trellis_gather_probe(lp, blocks, iters, sp, _stream(stream)), "trellis_gather_probe")
+    _check(_lib.load().trellis_gather_probe(lp, blocks, iters, replicas, sp, _stream(stream)),
+           "trellis_gather_probe")
     return sink
 
 

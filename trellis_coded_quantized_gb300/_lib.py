@@ -53,7 +53,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "trellis_expand": ([P, P, P, G, P, P, P], I32),
             "trellis_rmsnorm": ([P, I64, I64, ctypes.c_float, P, P], I32),
             "trellis_silu_mul": ([P, P, I64, P, P], I32),
-            "trellis_gather_probe": ([P, I32, I32, P, P], I32),
+            "trellis_gather_probe": ([P, I32, I32, I32, P, P], I32),
             "trellis_device_status": ([ctypes.POINTER(I32)], I32),
             "trellis_strerror": ([I32], ctypes.c_char_p),
         }

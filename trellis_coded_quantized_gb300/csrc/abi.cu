@@ -170,15 +170,16 @@ trellis_status trellis_silu_mul(const void* g, const void* u, int64_t n, void* o
                                          static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
 }
 
-trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t iters,
+trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t iters, int32_t replicas,
                                     float* sink, void* stream) {
     if (!lut || !sink) return TRELLIS_ERR_NULL;
     if (blocks < 1 || blocks > 65536 || iters < 1) return TRELLIS_ERR_SHAPE;
+    if (replicas != 1 && replicas != 4 && replicas != 8) return TRELLIS_ERR_SHAPE;
     if (!aligned16(lut)) return TRELLIS_ERR_ALIGN;
     const DeviceFacts* d;
     trellis_status st;
     if ((st = current_device(&d)) != TRELLIS_OK) return st;
-    return launched(tcq::launch_gather_probe(lut, blocks, iters, sink, static_cast<cudaStream_t>(stream)));
+    return launched(tcq::launch_gather_probe(lut, blocks, iters, replicas, sink, static_cast<cudaStream_t>(stream)));
 }
 
 trellis_status trellis_device_status(int32_t* status) {

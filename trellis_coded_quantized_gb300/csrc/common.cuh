@@ -41,6 +41,66 @@ __device__ __forceinline__ uint32_t win_off(const uint32_t* w, int i) {
     return f & 0x3FFCu;
 }
 
+// The same with the window placed at bit SH of the result: the byte offset of
+// entry win in a table whose entries are 2^SH bytes apart (SH = 5 for the
+// 8-way replicated codebook below, where the lane's copy is OR-ed in).
+template <int K, int SH>
+__device__ __forceinline__ uint32_t win_off_sh(const uint32_t* w, int i) {
+    const int b = K * i;
+    const int q = b >> 5;
+    const int s = b & 31;
+    uint32_t f;
+    if (s >= SH)
+        f = __funnelshift_r(w[q], w[q + 1], s - SH);
+    else if (q > 0)
+        f = __funnelshift_r(w[q - 1], w[q], 32 - SH + s);
+    else
+        f = w[0] << (SH - s);
+    return f & (0xFFFu << SH);
+}
+
+// 8-way replicated codebook: entry e of copy g at word 8e + g, so the copy
+// of lane group g = lane % 8 lives in banks {g, g+8, g+16, g+24} and the 4
+// lanes of a group only contend among themselves.  128 KB of shared memory.
+constexpr int kLutRep = 8;
+constexpr int kLutRepShift = 5;
+constexpr size_t kLutRepBytes = (size_t)kLutN * kLutRep * sizeof(float);
+
+__device__ __forceinline__ void stage_lut_rep8(float* lut_s, const float* __restrict__ lut) {
+    float4* dst = reinterpret_cast<float4*>(lut_s);
+    for (int e = threadIdx.x; e < kLutN; e += blockDim.x) {
+        const float v = __ldg(lut + e);
+        const float4 q = make_float4(v, v, v, v);
+        dst[2 * e] = q;
+        dst[2 * e + 1] = q;
+    }
+}
+
+// Byte offset of this lane's copy inside an entry of the replicated codebook.
+__device__ __forceinline__ uint32_t lut_rep_lane_offset() {
+    return (threadIdx.x & 7u) << 2;
+}
+
+// d += a.lo * b.lo (or .hi * .hi) with bf16 multiplicands and an f32
+// accumulator, rounded once: equal to converting both to f32 and fmaf.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+    return c;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+    return c;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ float lut_at(const float* lut_s, uint32_t byte_off) {
     return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(lut_s) + byte_off);
 }

@@ -42,14 +42,18 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ g, const uint16_t* 
 // Random 4-byte gathers from a 4096-entry shared-memory table: 8 independent
 // xorshift streams per thread, one gather per draw.  Each draw costs a few
 // integer operations, well under what the shared-memory port needs, so the
-// kernel runs at the gather rate of the SM.
+// kernel runs at the gather rate of the SM.  With REP = 8 (or 4) the table is
+// replicated so that lane group g = lane % REP only reads banks congruent to
+// g mod REP: entry e of copy g sits at word REP*e + g.
+template <int REP>
 __global__ void __launch_bounds__(1024, 1)
 gather_probe_kernel(const float* __restrict__ lut, int iters, float* __restrict__ sink) {
-    __shared__ __align__(16) float lut_s[kLutN];
-    stage_lut(lut_s, lut);
+    extern __shared__ __align__(16) float lut_s[];
+    for (int i = threadIdx.x; i < kLutN * REP; i += blockDim.x) lut_s[i] = __ldg(lut + i / REP);
     __syncthreads();
     uint32_t st[8];
     const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t gofs = (threadIdx.x % REP) * 4u;
     #pragma unroll
     for (int j = 0; j < 8; ++j) st[j] = 0x9E3779B9u * (tid * 8u + j + 1u);
     float acc = 0.f;
@@ -59,7 +63,8 @@ gather_probe_kernel(const float* __restrict__ lut, int iters, float* __restrict_
             st[j] ^= st[j] << 13;
             st[j] ^= st[j] >> 17;
             st[j] ^= st[j] << 5;
-            acc += lut_at(lut_s, st[j] & 0x3FFCu);
+            constexpr uint32_t mask = 0xFFFu * 4u * REP;
+            acc += lut_at(lut_s, (st[j] & mask) | gofs);
         }
     }
     sink[tid] = acc;
@@ -82,9 +87,22 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, float* sink,
+cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, int replicas, float* sink,
                                 cudaStream_t stream) {
-    gather_probe_kernel<<<(unsigned)blocks, 1024, 0, stream>>>(lut, iters, sink);
+    const size_t smem = (size_t)kLutN * replicas * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    switch (replicas) {
+        case 1: gather_probe_kernel<1><<<(unsigned)blocks, 1024, smem, stream>>>(lut, iters, sink); break;
+        case 4:
+            e = cudaFuncSetAttribute(gather_probe_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            gather_probe_kernel<4><<<(unsigned)blocks, 1024, smem, stream>>>(lut, iters, sink); break;
+        case 8:
+            e = cudaFuncSetAttribute(gather_probe_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            gather_probe_kernel<8><<<(unsigned)blocks, 1024, smem, stream>>>(lut, iters, sink); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int64_t M, int64_t D, float eps,
                            uint16_t* out, cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
                             uint16_t* out, cudaStream_t stream);
-cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, float* sink,
+cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, int replicas, float* sink,
                                 cudaStream_t stream);
 
 // Largest input width the matvec kernel accepts (one 32-column unit per thread).

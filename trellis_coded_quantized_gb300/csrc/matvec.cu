@@ -7,18 +7,20 @@
 // shuffle reduction of per-lane partial sums).
 //
 // GB300 layout of the work (warp FMA, no tensor cores at M = 1):
-//   - one CTA per SM, up to 640 threads, the 16 KB codebook in shared memory;
+//   - one CTA per SM, up to 640 threads; the codebook sits in shared memory
+//     as 8 interleaved copies (128 KB), lane group lane % 8 reading only its
+//     own 4 banks, which cuts the bank conflicts of the random gathers;
 //   - a "row group" of TG threads covers one whole row: thread t owns the
 //     32-column unit t of every row and keeps those 32 activations in
-//     registers as f32 for the whole kernel, so x is read once per CTA;
+//     registers as bf16 pairs for the whole kernel, so x is read once per CTA;
 //   - per row, a thread streams its unit's k words (one 16/8-byte load, or
-//     three 4-byte loads at k=3, coalesced across the warp), takes the
-//     neighbour word from the next lane with __shfl_sync, and does 32
-//     window extractions, codebook gathers, scale multiplies, bf16 roundings
-//     and FMAs;
+//     three 4-byte loads at k=3, coalesced across the warp; two rows ahead),
+//     takes the neighbour word from the next lane with __shfl_sync, and does
+//     32 window extractions, codebook gathers and scale multiplies, 16 paired
+//     bf16 roundings and 32 bf16 x bf16 -> f32 FMAs;
 //   - RB rows are accumulated side by side, then a butterfly reduce-scatter
-//     over the warp (RB-1+... shuffles for RB rows) and a sum over the warps
-//     of the group in shared memory produce the RB outputs.
+//     over the warp (RB shuffles for RB rows) and a sum over the warps of the
+//     group in shared memory produce the RB outputs.
 #include "common.cuh"
 #include "internal.h"
 
@@ -56,10 +58,10 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
               const uint16_t* __restrict__ scales, const float* __restrict__ lut,
               int rows, int units, int tg, int ng, uint16_t* __restrict__ out) {
     extern __shared__ __align__(16) float smem[];
-    float* lut_s = smem;
-    const int wg = tg >> 5;                       // warps per row group
-    float* red = smem + kLutN;                    // [2][ng][wg][kRB]
-    stage_lut(lut_s, lut);
+    float* lut_s = smem;                              // 8-way replicated codebook
+    const int wg = tg >> 5;                           // warps per row group
+    float* red = smem + kLutN * kLutRep;              // [2][ng][wg][kRB]
+    stage_lut_rep8(lut_s, lut);
 
     const int g = threadIdx.x / tg;
     const int t = threadIdx.x - g * tg;
@@ -67,25 +69,26 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const int wig = t >> 5;
     const bool active = t < units;
     const int64_t wpr = (int64_t)units * K;
+    const uint32_t gofs = lut_rep_lane_offset();
 
-    // activations of this thread's unit: window i <-> column c0 + 31 - i
-    float xf[32];
+    // activations of this thread's unit as bf16 pairs: xp[j] holds windows
+    // 2j (high half) and 2j+1 (low half), i.e. columns c0+31-2j and c0+30-2j
+    uint32_t xp[16];
     if (active) {
         const int c0 = (t >> 3) * kBT + (224 - 32 * (t & 7));
-        const uint4* xp = reinterpret_cast<const uint4*>(x + c0);
+        const uint4* src = reinterpret_cast<const uint4*>(x + c0);
         #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(xp + q);
-            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                xf[31 - (8 * q + 2 * j)] = bf16_bits_to_float(e[j] & 0xFFFFu);
-                xf[31 - (8 * q + 2 * j + 1)] = bf16_bits_to_float(e[j] >> 16);
-            }
+            const uint4 v = __ldg(src + q);
+            // word e of chunk q holds columns c0+8q+2e (lo) and c0+8q+2e+1 (hi)
+            xp[15 - 4 * q] = v.x;
+            xp[14 - 4 * q] = v.y;
+            xp[13 - 4 * q] = v.z;
+            xp[12 - 4 * q] = v.w;
         }
     } else {
         #pragma unroll
-        for (int i = 0; i < 32; ++i) xf[i] = 0.f;
+        for (int j = 0; j < 16; ++j) xp[j] = 0u;
     }
     __syncthreads();
 
@@ -95,41 +98,46 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const int src = next_unit_lane(lane);
     const uint32_t* tp = codes + (int64_t)t * K;
 
+    // two rows in flight ahead of the one being decoded
+    uint32_t pa[K], pb[K];
+    {
+        const int ra = r0 + g, rb = r0 + g + ng;
+        if (active && ra < r1) load_unit<K>(pa, tp + (int64_t)ra * wpr);
+        else {
+            #pragma unroll
+            for (int j = 0; j < K; ++j) pa[j] = 0u;
+        }
+        if (active && rb < r1) load_unit<K>(pb, tp + (int64_t)rb * wpr);
+        else {
+            #pragma unroll
+            for (int j = 0; j < K; ++j) pb[j] = 0u;
+        }
+    }
+
     int buf = 0;
     for (int j0 = 0; j0 < per_group; j0 += kRB, buf ^= 1) {
         float acc[kRB];
-        uint32_t nxt[K];
-        {
-            const int row = r0 + g + ng * j0;
-            if (active && row < r1) load_unit<K>(nxt, tp + (int64_t)row * wpr);
-            else {
-                #pragma unroll
-                for (int j = 0; j < K; ++j) nxt[j] = 0u;
-            }
-        }
         #pragma unroll
         for (int rho = 0; rho < kRB; ++rho) {
             const int row = r0 + g + ng * (j0 + rho);
             uint32_t w[K + 1];
             #pragma unroll
-            for (int j = 0; j < K; ++j) w[j] = nxt[j];
-            // prefetch the next row of the batch
-            if (rho + 1 < kRB) {
-                const int rn = row + ng;
-                if (active && rn < r1) load_unit<K>(nxt, tp + (int64_t)rn * wpr);
-            }
+            for (int j = 0; j < K; ++j) { w[j] = pa[j]; pa[j] = pb[j]; }
+            const int rn = row + 2 * ng;
+            if (active && rn < r1) load_unit<K>(pb, tp + (int64_t)rn * wpr);
             acc[rho] = 0.f;
             if (row < r1) {                              // uniform over the row group
                 w[K] = __shfl_sync(0xffffffffu, w[0], src);
                 const float s = bf16_bits_to_float(__ldg(scales + row));
                 float a0 = 0.f, a1 = 0.f;
                 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float v0 = lut_at(lut_s, win_off<K>(w, i));
-                    const float v1 = lut_at(lut_s, win_off<K>(w, i + 1));
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(v0, s), __fmul_rn(v1, s));
-                    a0 = fmaf(__low2float(h), xf[i], a0);
-                    a1 = fmaf(__high2float(h), xf[i + 1], a1);
+                for (int j = 0; j < 16; ++j) {
+                    const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j) | gofs);
+                    const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j + 1) | gofs);
+                    // pair laid out like xp[j]: window 2j high, window 2j+1 low
+                    const uint32_t wp = pack_bf16x2(__fmul_rn(v1, s), __fmul_rn(v0, s));
+                    a0 = fma_bf16_hi(wp, xp[j], a0);
+                    a1 = fma_bf16_lo(wp, xp[j], a1);
                 }
                 acc[rho] = a0 + a1;
             }
@@ -142,9 +150,9 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
         if (t < kRB) {
             const int row = r0 + g + ng * (j0 + t);
             if (row < r1) {
-                float s = 0.f;
-                for (int w = 0; w < wg; ++w) s += rb[((size_t)g * wg + w) * kRB + t];
-                out[row] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+                float sum = 0.f;
+                for (int w = 0; w < wg; ++w) sum += rb[((size_t)g * wg + w) * kRB + t];
+                out[row] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
             }
         }
         // the other buffer is written next; one barrier per batch suffices
@@ -162,7 +170,15 @@ cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
     const int threads = tg * ng;
     int grid = sm_count;
     if ((int64_t)grid > p.rows) grid = (int)p.rows;
-    const size_t smem = (size_t)(kLutN + 2 * ng * (tg / 32) * kRB) * sizeof(float);
+    const size_t smem = kLutRepBytes + (size_t)(2 * ng * (tg / 32) * kRB) * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    switch (p.k) {
+        case 2: e = cudaFuncSetAttribute(matvec_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
+        case 3: e = cudaFuncSetAttribute(matvec_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
+        case 4: e = cudaFuncSetAttribute(matvec_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
     switch (p.k) {
         case 2: matvec_kernel<2><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
         case 3: matvec_kernel<3><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;

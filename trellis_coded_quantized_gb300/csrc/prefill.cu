@@ -13,7 +13,8 @@
 //   - 8 decoder warps: warp w owns tensor-memory lane quarter w % 4 (32
 //     matrix rows, one row per thread) and half w / 4 of each 256-column
 //     block (4 units of 32 columns).  A thread streams its row's code words,
-//     extracts windows, gathers the codebook from shared memory, scales,
+//     extracts windows, gathers the codebook from shared memory (8-way
+//     replicated, one copy per lane group of 4, against bank conflicts), scales,
 //     rounds pairs to bf16x2 and writes them with tcgen05.st straight into
 //     the A stage: decoded weights never touch shared memory;
 //   - 1 loader warp copies the activation tile of each block into shared
@@ -45,7 +46,7 @@ struct PfLayout {
     static constexpr int kXStage = NPAD * kBT * 2;        // bytes of one activation stage
     static constexpr int kXChunk = NPAD * 128;            // one 64-column K chunk
     static constexpr int kLutOff = 2 * kXStage;
-    static constexpr int kBarOff = kLutOff + kLutN * 4;
+    static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
     static constexpr int kBytes = kBarOff + 64;
     static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
 };
@@ -92,7 +93,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    stage_lut(lut_s, lut);
+    stage_lut_rep8(lut_s, lut);
     if (threadIdx.x == 0) {
         tc::mbar_init(&full[0], kPfDecWarps * 32 + 32);
         tc::mbar_init(&full[1], kPfDecWarps * 32 + 32);
@@ -123,6 +124,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const float s = valid ? bf16_bits_to_float(__ldg(scales + row)) : 0.f;
         const uint32_t* rowp = codes + (int64_t)(valid ? row : 0) * nblocks * wpb;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        const uint32_t gofs = lut_rep_lane_offset();
         uint32_t cw[4 * K + 1], nw[4 * K + 1];
         load_half<K>(cw, rowp, h, valid);
         for (int b = 0; b < nblocks; ++b) {
@@ -140,8 +142,8 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 uint32_t r[16];
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float lo = lut_at(lut_s, win_off<K>(w, 31 - 2 * j));
-                    const float hi = lut_at(lut_s, win_off<K>(w, 30 - 2 * j));
+                    const float lo = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - 2 * j) | gofs);
+                    const float hi = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 30 - 2 * j) | gofs);
                     const __nv_bfloat162 p2 = __floats2bfloat162_rn(__fmul_rn(lo, s), __fmul_rn(hi, s));
                     r[j] = valid ? *reinterpret_cast<const uint32_t*>(&p2) : 0u;
                 }
