@@ -10,20 +10,27 @@
 //     weights (rows of the matrix are MMA rows, "swap AB") held in TENSOR
 //     MEMORY, B = activations in shared memory (K-major, 128-byte swizzle),
 //     D = fp32 accumulator in tensor memory; N = 16 or 32 (M padded);
-//   - 8 decoder warps: warp w owns tensor-memory lane quarter w % 4 (32
-//     matrix rows, one row per thread) and half w / 4 of each 256-column
-//     block (4 units of 32 columns).  A thread streams its row's code words,
+//   - 1 code-loader warp: per 256-column block it copies the block of all
+//     128 rows in coalesced 16-byte cp.async chunks (completion tracked on
+//     an mbarrier) into one of 3 shared-memory tiles whose row pitch is 16
+//     bytes more than a block, so 8 consecutive rows fall in 8 different
+//     bank groups; the decoders release a tile as soon as they hold its
+//     words, so the loads run up to 3 blocks ahead;
+//   - 1 activation-loader warp copies the activation tile of each block
+//     (cp.async, zero-filled rows M..N-1) into the swizzled layout;
+//   - 16 decoder warps: warp w owns tensor-memory lane quarter w % 4 (32
+//     matrix rows, one row per thread) and quarter w / 4 of each block (2
+//     units of 32 columns).  A thread reads its row's words from the tile,
 //     extracts windows, gathers the codebook from shared memory (8-way
-//     replicated, one copy per lane group of 4, against bank conflicts), scales,
-//     rounds pairs to bf16x2 and writes them with tcgen05.st straight into
-//     the A stage: decoded weights never touch shared memory;
-//   - 1 loader warp copies the activation tile of each block into shared
-//     memory in the swizzled layout;
+//     replicated, one copy per lane group of 4, against bank conflicts),
+//     scales, rounds pairs to bf16x2 and writes them with tcgen05.st straight
+//     into the A stage: decoded weights never touch shared memory;
 //   - 1 MMA warp: one thread waits for a stage, issues 16 tcgen05.mma
 //     (K = 16 each) and commits to the stage's "empty" barrier;
-//   - 2 stages (A: 2 x 128 tensor-memory columns, B: 2 x N x 512 bytes),
-//     mbarriers with bounded waits; after the last block the accumulator is
-//     read back with tcgen05.ld by the lane-quarter warps and stored as bf16.
+//   - 2 stages (A: 2 x 128 tensor-memory columns, B: 2 x N x 512 bytes,
+//     codes: 2 x 128 rows), mbarriers with bounded waits; after the last
+//     block the accumulator is read back with tcgen05.ld by the lane-quarter
+//     warps and stored as bf16.
 // The K order of a block is the natural column order on both operands.
 #include "common.cuh"
 #include "internal.h"
@@ -32,48 +39,54 @@
 namespace tcq {
 namespace {
 
-constexpr int kPfDecWarps = 8;
-constexpr int kPfMmaWarp = 8;
-constexpr int kPfLoadWarp = 9;
-constexpr int kPfThreads = 10 * 32;
+constexpr int kPfDecWarps = 16;            // 4 lane quarters x 4 block quarters
+constexpr int kPfParts = kPfDecWarps / 4;
+constexpr int kPfUnits = 8 / kPfParts;      // units of 32 columns per decoder warp and block
+constexpr int kPfMmaWarp = kPfDecWarps;
+constexpr int kPfLoadWarp = kPfDecWarps + 1;      // activation tiles
+constexpr int kPfCodeWarp = kPfDecWarps + 2;      // code tiles
+constexpr int kPfThreads = (kPfDecWarps + 3) * 32;
+constexpr int kPfCodeStages = 3;
 constexpr int kPfRows = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator columns [256, 256 + N)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-template <int NPAD>
+template <int K, int NPAD>
 struct PfLayout {
-    static constexpr int kXStage = NPAD * kBT * 2;        // bytes of one activation stage
-    static constexpr int kXChunk = NPAD * 128;            // one 64-column K chunk
-    static constexpr int kLutOff = 2 * kXStage;
+    static constexpr int kWpb = kBT * K / 32;              // words of one block
+    static constexpr int kPitch = kWpb * 4 + 16;           // bytes per row of a code tile
+    static constexpr int kXStage = NPAD * kBT * 2;         // bytes of one activation stage
+    static constexpr int kXChunk = NPAD * 128;             // one 64-column K chunk
+    static constexpr int kCodeOff = 2 * kXStage;
+    static constexpr int kCodeStage = kPfRows * kPitch;
+    static constexpr int kLutOff = kCodeOff + kPfCodeStages * kCodeStage;
     static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
-    static constexpr int kBytes = kBarOff + 64;
-    static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
+    static constexpr int kBytes = kBarOff + 128;
+    static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
 };
 
-__device__ __forceinline__ uint4 ld_nc_v4(const uint32_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-// Words of one half block of one row: 4 units (4K words) and the neighbour.
+// Words of the kPfUnits units of one block quarter of one row from the
+// shared code tile, plus the neighbour word (first word of the next unit,
+// unit 0 for the last quarter).
 template <int K>
-__device__ __forceinline__ void load_half(uint32_t* w, const uint32_t* blk, int h, bool valid) {
-    if (!valid) {
+__device__ __forceinline__ void read_quarter(uint32_t* w, const uint8_t* row, int part) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + part * kPfUnits * K;
+    if constexpr (K == 3) {
         #pragma unroll
-        for (int j = 0; j < 4 * K + 1; ++j) w[j] = 0u;
-        return;
+        for (int j = 0; j < kPfUnits * K; j += 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(p + j);
+            w[j] = v.x; w[j + 1] = v.y;
+        }
+    } else {
+        #pragma unroll
+        for (int j = 0; j < kPfUnits * K; j += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p + j);
+            w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+        }
     }
-    const uint32_t* p = blk + 4 * h * K;
-    #pragma unroll
-    for (int q = 0; q < K; ++q) {
-        const uint4 v = ld_nc_v4(p + 4 * q);
-        w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-    }
-    // neighbour of unit 4h+3: unit 4 of the block, or unit 0 (wrap) for h = 1
-    w[4 * K] = __ldg(blk + (h == 0 ? 4 * K : 0));
+    const int nb = (part + 1 == kPfParts) ? 0 : (part + 1) * kPfUnits * K;
+    w[kPfUnits * K] = reinterpret_cast<const uint32_t*>(row)[nb];
 }
 
 template <int K, int NPAD>
@@ -81,24 +94,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
                int rows, int cols, uint16_t* __restrict__ out, int* __restrict__ status) {
-    using Lay = PfLayout<NPAD>;
+    using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xs = base;
+    uint8_t* cs = base + Lay::kCodeOff;
     float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);
-    uint64_t* empty = full + 2;
-    uint64_t* done = full + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);   // decoders + activations
+    uint64_t* empty = full + 2;                                           // MMA done with a stage
+    uint64_t* cfull = full + 4;                                           // code tile landed [3]
+    uint64_t* cempty = full + 7;                                          // code tile read [3]
+    uint64_t* done = full + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 11);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     stage_lut_rep8(lut_s, lut);
     if (threadIdx.x == 0) {
-        tc::mbar_init(&full[0], kPfDecWarps * 32 + 32);
-        tc::mbar_init(&full[1], kPfDecWarps * 32 + 32);
-        tc::mbar_init(&empty[0], 1);
-        tc::mbar_init(&empty[1], 1);
+        for (int st = 0; st < 2; ++st) {
+            tc::mbar_init(&full[st], kPfDecWarps * 32 + 32);
+            tc::mbar_init(&empty[st], 1);
+        }
+        for (int st = 0; st < kPfCodeStages; ++st) {
+            tc::mbar_init(&cfull[st], 32);
+            tc::mbar_init(&cempty[st], kPfDecWarps * 32);
+        }
         tc::mbar_init(done, 1);
         *abort_flag = 0;
         tc::mbar_init_fence();
@@ -113,29 +133,31 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     const uint32_t tmem = *tmem_slot;
 
     const int nblocks = cols / kBT;
-    constexpr int wpb = kBT * K / 32;
+    constexpr int wpb = Lay::kWpb;
     const int row0 = blockIdx.x * kPfRows;
+    const int nvalid = min(kPfRows, rows - row0);
 
     if (warp < kPfDecWarps) {
         // ------------------------------------------------------------ decoders
-        const int q = warp & 3, h = warp >> 2;
-        const int row = row0 + 32 * q + lane;
-        const bool valid = row < rows;
-        const float s = valid ? bf16_bits_to_float(__ldg(scales + row)) : 0.f;
-        const uint32_t* rowp = codes + (int64_t)(valid ? row : 0) * nblocks * wpb;
+        const int q = warp & 3, part = warp >> 2;
+        const int rl = 32 * q + lane;
+        const bool valid = rl < nvalid;
+        const float s = valid ? bf16_bits_to_float(__ldg(scales + row0 + rl)) : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t gofs = lut_rep_lane_offset();
-        uint32_t cw[4 * K + 1], nw[4 * K + 1];
-        load_half<K>(cw, rowp, h, valid);
         for (int b = 0; b < nblocks; ++b) {
             const int stage = b & 1;
-            if (b + 1 < nblocks) load_half<K>(nw, rowp + (int64_t)(b + 1) * wpb, h, valid);
+            const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
+            if (!tc::mbar_wait(&cfull[cst], cuse & 1, abort_flag, kWaitLimitNs)) break;
+            uint32_t cw[kPfUnits * K + 1];
+            read_quarter<K>(cw, cs + cst * Lay::kCodeStage + rl * Lay::kPitch, part);
+            tc::mbar_arrive(&cempty[cst]);                 // the code tile may be refilled
             if (b >= 2 && !tc::mbar_wait(&empty[stage], ((b >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) break;
             __syncwarp();
             tc::tc_fence_after();
             #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                const int u = 4 * h + uu;
+            for (int uu = 0; uu < kPfUnits; ++uu) {
+                const int u = kPfUnits * part + uu;
                 uint32_t w[K + 1];
                 #pragma unroll
                 for (int j = 0; j <= K; ++j) w[j] = cw[uu * K + j];   // neighbour is the next unit's first word
@@ -144,22 +166,45 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 for (int j = 0; j < 16; ++j) {
                     const float lo = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - 2 * j) | gofs);
                     const float hi = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 30 - 2 * j) | gofs);
-                    const __nv_bfloat162 p2 = __floats2bfloat162_rn(__fmul_rn(lo, s), __fmul_rn(hi, s));
-                    r[j] = valid ? *reinterpret_cast<const uint32_t*>(&p2) : 0u;
+                    const uint32_t p2 = pack_bf16x2(__fmul_rn(lo, s), __fmul_rn(hi, s));
+                    r[j] = valid ? p2 : 0u;
                 }
                 tc::tmem_st16(lane_base + (uint32_t)(stage * 128 + 112 - 16 * u), r);
             }
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&full[stage]);
-            #pragma unroll
-            for (int j = 0; j < 4 * K + 1; ++j) cw[j] = nw[j];
+        }
+    } else if (warp == kPfCodeWarp) {
+        // ------------------------------------------------------------ code loader
+        // The block of all valid rows in 16-byte cp.async chunks (a warp
+        // instruction covers 512 contiguous bytes of consecutive rows) into
+        // tile cst; each lane's copies arrive on cfull[cst] when they land.
+        // Up to kPfCodeStages blocks ahead of the decoders, which release a
+        // tile (cempty) as soon as they hold its words in registers.
+        const int64_t wpr = (int64_t)nblocks * wpb;
+        constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
+        const int nchunks = nvalid * cpr;
+        for (int b = 0; b < nblocks; ++b) {
+            const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
+            if (b >= kPfCodeStages &&
+                !tc::mbar_wait(&cempty[cst], (cuse - 1) & 1, abort_flag, kWaitLimitNs)) break;
+            const uint32_t ct = tc::smem_addr(cs + cst * Lay::kCodeStage);
+            const uint32_t* src0 = codes + (int64_t)row0 * wpr + (int64_t)b * wpb;
+            for (int c = lane; c < nchunks; c += 32) {
+                const int r = c / cpr, part = c - (c / cpr) * cpr;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(ct + r * Lay::kPitch + part * 16), "l"(src0 + (int64_t)r * wpr + part * 4)
+                             : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                         :: "r"(tc::smem_addr(&cfull[cst])) : "memory");
         }
     } else if (warp == kPfLoadWarp) {
         // ------------------------------------------------------------ activation loader
         // 16-byte cp.async copies into the swizzled layout (rows >= M are
         // zero-filled); the warp waits for its own copies, then fences them
-        // into the async proxy before arriving.
+        // into the async proxy before arriving on full[stage].
         const uint32_t xs_base = tc::smem_addr(xs);
         for (int b = 0; b < nblocks; ++b) {
             const int stage = b & 1;
@@ -236,7 +281,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
 template <int K, int NPAD>
 cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, int* status,
                       cudaStream_t stream) {
-    const int smem = PfLayout<NPAD>::kAlloc;
+    const int smem = PfLayout<K, NPAD>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<K, NPAD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -7,15 +7,18 @@
 // C] float partials and their sum over the split axis, cast to bf16).
 //
 // GB300 layout of the work:
-//   - a lane owns one 32-column unit of the output columns and walks the rows
-//     of its split: per row it streams the unit's k words (coalesced over the
-//     warp: 32 lanes cover 4 consecutive blocks), takes the neighbour word
-//     by __shfl_sync, decodes 32 weights and does MB FMAs per weight, one per
-//     activation row (the shared-M variants of scatter.ts share each decoded
-//     weight across activation rows the same way);
-//   - the 4 warps of a CTA take interleaved rows of the same (split, column
-//     range) and their partial sums are added in shared memory before the
-//     store, so a CTA writes one [MB, 1024] slab of partials;
+//   - one CTA per SM owns one split and a block of up to 5 column ranges of
+//     1024 columns; the 8-way replicated codebook (128 KB) sits in its
+//     shared memory;
+//   - a lane owns one 32-column unit and walks the rows of the split: per
+//     row it streams the unit's k words (coalesced over the warp: 32 lanes
+//     cover 4 consecutive blocks), takes the neighbour word by __shfl_sync,
+//     decodes 32 weights and does MB FMAs per weight (bf16 x bf16 into f32),
+//     one per activation row -- the shared-M variants of scatter.ts share
+//     each decoded weight across activation rows the same way;
+//   - RW warps per column range take interleaved rows of the split and their
+//     partial sums are added in shared memory, in warp order, before the
+//     store of the [MB, 1024] slab of partials;
 //   - more than 4 activation rows are processed in passes of up to 4.
 #include "common.cuh"
 #include "internal.h"
@@ -23,31 +26,40 @@
 namespace tcq {
 namespace {
 
-constexpr int kScWarps = 4;       // warps per CTA, sharing rows of one split
-constexpr int kScThreads = kScWarps * 32;
+// Row warps per column range: 4 with one activation row, else 2; warps per
+// CTA at most 20 (one activation row) or 10 (the accumulators of 2..4 rows
+// need the larger register share).
+__host__ __device__ constexpr int sc_row_warps(int mb) { return mb == 1 ? 4 : 2; }
+__host__ __device__ constexpr int sc_max_warps(int mb) { return mb == 1 ? 20 : 10; }
 
 template <int K, int MB>
-__global__ void __launch_bounds__(kScThreads)
+__global__ void __launch_bounds__(sc_max_warps(MB) * 32, 1)
 scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-               int R, int C, int splits, int rp, int nur, float* __restrict__ partial) {
+               int R, int C, int splits, int rp, int nur, int nurb, float* __restrict__ partial) {
+    constexpr int RW = sc_row_warps(MB);
     extern __shared__ __align__(16) float smem[];
-    float* lut_s = smem;
-    float* red = smem + kLutN;             // [kScWarps-1][MB][32 lanes][32 cols]
-    stage_lut(lut_s, lut);
+    float* lut_s = smem;                                // 8-way replicated codebook
+    float* red = smem + kLutN * kLutRep;                // [RW-1][nurb][MB][32 cols][32 lanes]
+    stage_lut_rep8(lut_s, lut);
     __syncthreads();
 
-    const int s = blockIdx.x / nur;        // split
-    const int ur = blockIdx.x - s * nur;   // range of 32 units = 1024 columns
+    const int nblk = (nur + nurb - 1) / nurb;
+    const int s = blockIdx.x / nblk;                    // split
+    const int ub = blockIdx.x - s * nblk;               // block of column ranges
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int url = warp % nurb;                        // column range within the block
+    const int rwi = warp / nurb;                        // row warp
+    const int ur = ub * nurb + url;
     const int units = C >> 5;
     const int unit = ur * 32 + lane;
-    const bool active = unit < units;
+    const bool active = ur < nur && unit < units;
     const int r0 = s * rp;
     const int r1 = min(R, r0 + rp);
     const int64_t wpr = (int64_t)units * K;
-    const uint32_t* tp = codes + (int64_t)unit * K;
+    const uint32_t* tp = codes + (int64_t)(active ? unit : 0) * K;
     const int src = next_unit_lane(lane);
+    const uint32_t gofs = lut_rep_lane_offset();
 
     float acc[MB][32];
     #pragma unroll
@@ -56,50 +68,57 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
         for (int i = 0; i < 32; ++i) acc[m][i] = 0.f;
 
     uint32_t nxt[K];
-    int r = r0 + warp;
+    #pragma unroll
+    for (int j = 0; j < K; ++j) nxt[j] = 0u;
+    int r = r0 + rwi;
     if (active && r < r1) load_unit<K>(nxt, tp + (int64_t)r * wpr);
-    for (; r < r1; r += kScWarps) {
+    for (; r < r1; r += RW) {
         uint32_t w[K + 1];
         #pragma unroll
         for (int j = 0; j < K; ++j) w[j] = nxt[j];
-        const int rn = r + kScWarps;
+        const int rn = r + RW;
         if (active && rn < r1) load_unit<K>(nxt, tp + (int64_t)rn * wpr);
         w[K] = __shfl_sync(0xffffffffu, w[0], src);
         const float sr = bf16_bits_to_float(__ldg(scales + r));
-        float xr[MB];
+        uint32_t xx[MB];                                // x[m][r] in both halves
         #pragma unroll
-        for (int m = 0; m < MB; ++m) xr[m] = bf16_bits_to_float(__ldg(x + (int64_t)(m0 + m) * R + r));
+        for (int m = 0; m < MB; ++m) {
+            const uint32_t h = __ldg(x + (int64_t)(m0 + m) * R + r);
+            xx[m] = h | (h << 16);
+        }
         #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-            const float v0 = lut_at(lut_s, win_off<K>(w, i));
-            const float v1 = lut_at(lut_s, win_off<K>(w, i + 1));
-            const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(v0, sr), __fmul_rn(v1, sr));
-            const float w0 = __low2float(h), w1 = __high2float(h);
+            const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i) | gofs);
+            const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i + 1) | gofs);
+            const uint32_t wp = pack_bf16x2(__fmul_rn(v0, sr), __fmul_rn(v1, sr));
             #pragma unroll
             for (int m = 0; m < MB; ++m) {
-                acc[m][i] = fmaf(w0, xr[m], acc[m][i]);
-                acc[m][i + 1] = fmaf(w1, xr[m], acc[m][i + 1]);
+                acc[m][i] = fma_bf16_lo(wp, xx[m], acc[m][i]);
+                acc[m][i + 1] = fma_bf16_hi(wp, xx[m], acc[m][i + 1]);
             }
         }
     }
 
-    // add the warps' partial sums (warps 1..3 stage theirs, warp 0 adds in order)
-    if (warp > 0) {
-        float* dst = red + (size_t)(warp - 1) * MB * 1024;
+    // add the row warps' partial sums (row warps 1.. stage theirs, row warp 0
+    // adds them in order) and store the slab
+    if (rwi > 0) {
+        float* dst = red + ((size_t)(rwi - 1) * nurb + url) * MB * 1024;
         #pragma unroll
         for (int m = 0; m < MB; ++m)
             #pragma unroll
             for (int i = 0; i < 32; ++i) dst[(m * 32 + i) * 32 + lane] = acc[m][i];
     }
     __syncthreads();
-    if (warp == 0 && active) {
+    if (rwi == 0 && active) {
         #pragma unroll
         for (int m = 0; m < MB; ++m) {
             float v[32];
             #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 float a = acc[m][i];
-                for (int w = 0; w < kScWarps - 1; ++w) a += red[((size_t)w * MB * 32 + m * 32 + i) * 32 + lane];
+                #pragma unroll
+                for (int q = 1; q < RW; ++q)
+                    a += red[(((size_t)(q - 1) * nurb + url) * MB * 32 + m * 32 + i) * 32 + lane];
                 v[i] = a;
             }
             // window i <-> column c0 + 31 - i
@@ -112,31 +131,31 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
     }
 }
 
-// out[m][c] = bf16( sum_s partial[m][s][c] ): a CTA covers 128 columns of one
-// activation row; 8 thread groups each add a contiguous run of splits in
-// order, and the 8 runs are then added in order.
-constexpr int kRdGroups = 8;
+// out[m][c] = bf16( sum_s partial[m][s][c] ): a CTA covers 32 columns of one
+// activation row with 32 groups of 8 threads; group g adds a contiguous run
+// of splits in order (4 runs of 4 rows of 128 bytes for 128 splits), then
+// the 32 runs are added in order.
+constexpr int kRdGroups = 32;
+constexpr int kRdCols = 32;
 
 __global__ void __launch_bounds__(256)
 split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16_t* __restrict__ out) {
-    __shared__ float4 red[kRdGroups][32];
+    __shared__ float4 red[kRdGroups][kRdCols / 4];
     const int m = blockIdx.y;
-    const int cq = blockIdx.x * 32 + (threadIdx.x & 31);   // float4 column index
-    const int grp = threadIdx.x >> 5;
+    const int cq = blockIdx.x * (kRdCols / 4) + (threadIdx.x & 7);   // float4 column index
+    const int grp = threadIdx.x >> 3;
     const int per = (splits + kRdGroups - 1) / kRdGroups;
     const int s0 = grp * per, s1 = min(splits, s0 + per);
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (cq * 4 < C) {
-        const float4* p = reinterpret_cast<const float4*>(partial + (int64_t)m * splits * C) + cq;
-        const int64_t stride = C / 4;
-        for (int s = s0; s < s1; ++s) {
-            const float4 v = __ldg(p + (int64_t)s * stride);
-            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-        }
+    const float4* p = reinterpret_cast<const float4*>(partial + (int64_t)m * splits * C) + cq;
+    const int64_t stride = C / 4;
+    for (int s = s0; s < s1; ++s) {
+        const float4 v = __ldg(p + (int64_t)s * stride);
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
     }
-    red[grp][threadIdx.x & 31] = a;
+    red[grp][threadIdx.x & 7] = a;
     __syncthreads();
-    if (grp == 0 && cq * 4 < C) {
+    if (grp == 0) {
         float4 t = red[0][threadIdx.x];
         for (int g = 1; g < kRdGroups; ++g) {
             const float4 v = red[g][threadIdx.x];
@@ -154,17 +173,17 @@ split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16
 template <int K, int MB>
 cudaError_t launch_pass(const Packed& p, const uint16_t* x, int m0, int splits, int rp, int nur,
                         float* partial, cudaStream_t stream) {
-    const size_t smem = (size_t)(kLutN + (kScWarps - 1) * MB * 1024) * sizeof(float);
-    static bool configured = false;   // per template instance; benign race (idempotent)
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(scatter_kernel<K, MB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    const unsigned grid = (unsigned)(splits * nur);
-    scatter_kernel<K, MB><<<grid, kScThreads, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
-                                                              (int)p.rows, (int)p.cols, splits, rp, nur, partial);
+    constexpr int RW = sc_row_warps(MB);
+    const int nurb = nur < sc_max_warps(MB) / RW ? nur : sc_max_warps(MB) / RW;
+    const int nblk = (nur + nurb - 1) / nurb;
+    const size_t smem = kLutRepBytes + (size_t)(RW - 1) * nurb * MB * 1024 * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(scatter_kernel<K, MB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(splits * nblk);
+    scatter_kernel<K, MB><<<grid, nurb * RW * 32, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
+                                                                  (int)p.rows, (int)p.cols, splits, rp,
+                                                                  nur, nurb, partial);
     return cudaGetLastError();
 }
 
@@ -202,7 +221,7 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     }
     if (e != cudaSuccess) return e;
     const int C = (int)p.cols;
-    dim3 grid((unsigned)((C / 4 + 31) / 32), (unsigned)M);
+    dim3 grid((unsigned)(C / kRdCols), (unsigned)M);
     split_reduce_kernel<<<grid, 256, 0, stream>>>(partial, splits, C, out);
     return cudaGetLastError();
 }
