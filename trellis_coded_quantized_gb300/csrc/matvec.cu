@@ -61,6 +61,7 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     float* lut_s = smem;                              // 8-way replicated codebook
     const int wg = tg >> 5;                           // warps per row group
     float* red = smem + kLutN * kLutRep;              // [2][ng][wg][kRB]
+    stage_lut_rep8(lut_s, lut);
 
     const int g = threadIdx.x / tg;
     const int t = threadIdx.x - g * tg;
@@ -69,29 +70,6 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const bool active = t < units;
     const int64_t wpr = (int64_t)units * K;
     const uint32_t gofs = lut_rep_lane_offset();
-
-    const int r0 = (int)((int64_t)rows * blockIdx.x / gridDim.x);
-    const int r1 = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
-    const int per_group = (r1 - r0 + ng - 1) / ng;
-    const int src = next_unit_lane(lane);
-    const uint32_t* tp = codes + (int64_t)t * K;
-
-    // two rows in flight ahead of the one being decoded; issued first so
-    // that their latency overlaps the activation loads and the codebook staging
-    uint32_t pa[K], pb[K];
-    {
-        const int ra = r0 + g, rb = r0 + g + ng;
-        if (active && ra < r1) load_unit<K>(pa, tp + (int64_t)ra * wpr);
-        else {
-            #pragma unroll
-            for (int j = 0; j < K; ++j) pa[j] = 0u;
-        }
-        if (active && rb < r1) load_unit<K>(pb, tp + (int64_t)rb * wpr);
-        else {
-            #pragma unroll
-            for (int j = 0; j < K; ++j) pb[j] = 0u;
-        }
-    }
 
     // activations of this thread's unit as bf16 pairs: xp[j] holds windows
     // 2j (high half) and 2j+1 (low half), i.e. columns c0+31-2j and c0+30-2j
@@ -112,8 +90,29 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
         #pragma unroll
         for (int j = 0; j < 16; ++j) xp[j] = 0u;
     }
-    stage_lut_rep8(lut_s, lut);
     __syncthreads();
+
+    const int r0 = (int)((int64_t)rows * blockIdx.x / gridDim.x);
+    const int r1 = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
+    const int per_group = (r1 - r0 + ng - 1) / ng;
+    const int src = next_unit_lane(lane);
+    const uint32_t* tp = codes + (int64_t)t * K;
+
+    // two rows in flight ahead of the one being decoded
+    uint32_t pa[K], pb[K];
+    {
+        const int ra = r0 + g, rb = r0 + g + ng;
+        if (active && ra < r1) load_unit<K>(pa, tp + (int64_t)ra * wpr);
+        else {
+            #pragma unroll
+            for (int j = 0; j < K; ++j) pa[j] = 0u;
+        }
+        if (active && rb < r1) load_unit<K>(pb, tp + (int64_t)rb * wpr);
+        else {
+            #pragma unroll
+            for (int j = 0; j < K; ++j) pb[j] = 0u;
+        }
+    }
 
     int buf = 0;
     for (int j0 = 0; j0 < per_group; j0 += kRB, buf ^= 1) {

@@ -96,7 +96,10 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                int rows, int cols, uint16_t* __restrict__ out, int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic on the shared
+    // array (an integer round trip would lose the shared address space and
+    // turn every table gather into a generic load)
+    uint8_t* base = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* xs = base;
     uint8_t* cs = base + Lay::kCodeOff;
     float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
