@@ -183,7 +183,9 @@ class Workload:
             self.kernel_file = "prefill.cu"
         elif w == "scatter":
             self.M, self.K, self.N, self.k, self.axis = args.M or 1, 17408, 5120, 3, 0
-            self.desc = f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, 128 splits"
+            self.splits = getattr(args, "splits", 0) or 128
+            self.desc = (f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, "
+                         f"{self.splits} splits")
             self.kernel = "scatter_kernel<3> + split_reduce_kernel"
             self.kernel_file = "scatter.cu"
         else:
@@ -202,13 +204,13 @@ class Workload:
         self.out = torch.empty((self.M, nout), dtype=torch.bfloat16, device=device)
         self.ws = None
         if w == "scatter":
-            self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(self.g, self.M, 128) // 4,
+            self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(self.g, self.M, self.splits) // 4,
                                   dtype=torch.float32, device=device)
         # algorithmic bytes of the dominant launch: codes, scales, codebook, x, out
         self.alg_bytes = self.packed + rows * 2 + 4096 * 4 + self.M * (cols if self.axis == 1 else rows) * 2 \
             + self.M * nout * 2
         if w == "scatter":   # the split partials are written and read back once
-            self.alg_bytes += 2 * self.M * 128 * cols * 4
+            self.alg_bytes += 2 * self.M * self.splits * cols * 4
         self.launches_per_step = 1 if w != "scatter" else 1 + (self.M + 3) // 4
 
     def run(self, codes, x=None, out=None):
@@ -220,7 +222,8 @@ class Workload:
         elif self.name == "prefill":
             tcq.trellis_prefill(x, codes, self.scales, self.lut, self.g, out=out)
         else:
-            tcq.trellis_scatter(x, codes, self.scales, self.lut, self.g, splits=128, workspace=self.ws, out=out)
+            tcq.trellis_scatter(x, codes, self.scales, self.lut, self.g, splits=self.splits, workspace=self.ws,
+                                out=out)
 
     def step(self, i):
         self.run(self.sets[i % self.nsets])
@@ -257,14 +260,15 @@ def secondary(torch, tcq, device, stream, peaks, l2):
 
     class A:
         pass
-    for w, M, k in ([("prefill", M, k) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
-                    [("scatter", 1, 3), ("scatter", 4, 3), ("tiny-matvec", 1, 2)]):
+    for w, M, k, S in ([("prefill", M, k, 0) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
+                       [("scatter", 1, 3, 128), ("scatter", 4, 3, 128), ("scatter", 1, 3, 152),
+                        ("scatter", 4, 3, 152), ("tiny-matvec", 1, 2, 0)]):
         a = A()
-        a.workload, a.M, a.k = w, M, k
+        a.workload, a.M, a.k, a.splits = w, M, k, S
         wl = Workload(a, torch, tcq, device, l2)
         _, per = time_launches(torch, wl.step, 30, 3, stream, lambda: None)
         t = statistics.median(per) * 1e-3
-        key = f"{w}_M{M}_k{k}"
+        key = f"{w}_M{M}_k{k}" + (f"_s{S}" if w == "scatter" else "")
         rec = {"us": round(t * 1e6, 2), "packed_gbs": round(wl.packed / t / 1e9, 1),
                "tokens_per_s": round(M / t, 1), "frac_of_hbm_alg": round(wl.alg_bytes / t / 1e9 / hbm, 4)}
         if w == "prefill":
@@ -510,6 +514,7 @@ def main():
                     default="decode-matvec")
     ap.add_argument("--M", type=int, default=0, help="activation rows (prefill: 32, scatter: 1)")
     ap.add_argument("--k", type=int, default=0, help="bits per symbol of the prefill (4)")
+    ap.add_argument("--splits", type=int, default=0, help="row splits of the scatter (128)")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
