@@ -286,10 +286,28 @@ def secondary(torch, tcq, device, stream, peaks, l2):
         x0 = torch.from_numpy(synth.activations(0, M, 5120).view(np.int16)).to(device).view(torch.bfloat16)
         _, per = time_launches(torch, lambda i: stack.forward(x0), 5, 2, stream, lambda: None)
         t = statistics.median(per) * 1e-3
-        out[f"mlp40_M{M}_k3"] = {"ms_per_pass": round(t * 1e3, 3), "tokens_per_s": round(M / t, 1),
-                                 "packed_gbs": round(stack.packed_bytes / t / 1e9, 1),
-                                 "tflops": round(2.0 * M * stack.packed_bytes * 8 / 3 / t / 1e12, 2),
-                                 "launches_per_pass": stack.launches_per_pass(M)}
+        rec = {"ms_per_pass": round(t * 1e3, 3), "tokens_per_s": round(M / t, 1),
+               "packed_gbs": round(stack.packed_bytes / t / 1e9, 1),
+               "tflops": round(2.0 * M * stack.packed_bytes * 8 / 3 / t / 1e12, 2),
+               "launches_per_pass": stack.launches_per_pass(M)}
+        # the same pass captured once in a CUDA graph and replayed
+        try:
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                stack.forward(x0)
+            torch.cuda.current_stream().wait_stream(side)
+            with torch.cuda.graph(graph):
+                stack.forward(x0)
+            _, per = time_launches(torch, lambda i: graph.replay(), 5, 2, stream, lambda: None)
+            tg = statistics.median(per) * 1e-3
+            rec["graph_ms_per_pass"] = round(tg * 1e3, 3)
+            rec["graph_tokens_per_s"] = round(M / tg, 1)
+            del graph
+        except Exception as e:          # report, do not fail the bench line
+            rec["graph_error"] = str(e)[:200]
+        out[f"mlp40_M{M}_k3"] = rec
     del stack
     torch.cuda.empty_cache()
     # shared-memory gather rate (the decode's second roofline), with 1, 4 and 8 table copies

@@ -27,7 +27,8 @@
  *     argument returns an error status before anything is enqueued; no
  *     kernel traps or asserts.  Kernel-side waits are bounded: a wait that
  *     gives up records a code readable with trellis_device_status().
- *   - codes are uint32 [rows, (cols/256)*wpb] (interleave 0).  scales are
+ *   - codes are rows*(cols/256)*wpb uint32 words in the geometry's block
+ *     layout (see trellis_geometry).  scales are
  *     bf16 [rows].  lut is f32 [4096].  codes and x must be 16-byte aligned.
  */
 #ifndef TRELLIS_H
@@ -48,8 +49,14 @@ extern "C" {
  *   axis 0: rows are input features, cols are output features
  *           (out[m][c] = sum_r x[m][r] w[r][c]; scatter.ts).
  *   bt must be 256, L must be 12, k in {2, 3, 4}, rows >= 1,
- *   cols a positive multiple of 256.  interleave must be 0 (contiguous
- *   blocks; the pages' interleave-2 layout is not accepted).
+ *   cols a positive multiple of 256.
+ *   interleave 0: the blocks of a row are contiguous; block b of row r
+ *                 starts at word (r*(cols/256) + b)*wpb.
+ *   interleave 2: blocks are grouped in pairs and the pair of every row is
+ *                 stored together; block b of row r starts at word
+ *                 (b/2)*rows*2*wpb + r*2*wpb + (b%2)*wpb (vector-expand.ts
+ *                 and scatter.ts, INTERLEAVE).  cols must then be a multiple
+ *                 of 512.  Same number of words as interleave 0.
  */
 typedef struct trellis_geometry {
     int32_t axis;

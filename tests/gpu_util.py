@@ -23,7 +23,7 @@ def host_bf16(t) -> np.ndarray:
 
 
 def on_device(p: dict) -> dict:
-    g = tcq.geometry(p["axis"], p["rows"], p["cols"], p["k"])
+    g = tcq.geometry(p["axis"], p["rows"], p["cols"], p["k"], p.get("interleave", 0))
     return {"g": g, "codes": dev(p["codes"]), "scales": dev(p["scales"]), "lut": dev(p["lut"]),
             "x": dev(p["x"])}
 

@@ -63,7 +63,8 @@ def test_null_pointers(lib):
     assert lib.trellis_device_status(None) == NULL
 
 
-@pytest.mark.parametrize("field,value", [("bt", 128), ("L", 11), ("k", 1), ("k", 5), ("interleave", 2),
+@pytest.mark.parametrize("field,value", [("bt", 128), ("L", 11), ("k", 1), ("k", 5), ("interleave", 1),
+                                         ("interleave", 3),
                                          ("cols", 300), ("cols", 0), ("rows", 0), ("axis", 2)])
 def test_bad_geometry(lib, field, value):
     g = geometry(1, 256, 512, 2)
@@ -119,3 +120,10 @@ def test_glue_validation(lib):
     assert lib.trellis_gather_probe(_p(A), 0, 1, 1, _p(A), None) == SHAPE
     assert lib.trellis_gather_probe(_p(A), 1, 1, 3, _p(A), None) == SHAPE
     assert lib.trellis_gather_probe(_p(U), 1, 1, 1, _p(A), None) == ALIGN
+
+
+def test_interleave_two_needs_an_even_block_count(lib):
+    g = geometry(1, 256, 768, 2, interleave=2)      # 3 blocks
+    assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == GEOM
+    g = geometry(1, 256, 512, 2, interleave=2)      # 2 blocks: passes validation up to alignment
+    assert lib.trellis_matvec(_p(U), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == ALIGN

@@ -217,6 +217,72 @@ def test_scatter_unit_vectors_exact(orc, k):
         assert np.array_equal(out[0], W[r]), r
 
 
+# ----------------------------------------------------------------- interleave-2 layout
+
+def _inter(p):
+    p = dict(p)
+    p["interleave"] = 2
+    return p
+
+
+@pytest.mark.parametrize("axis,rows,cols,k", [(0, 17408, 5120, 3), (1, 300, 1024, 4), (0, 37, 512, 2)])
+def test_expand_interleave2_bit_exact(orc, axis, rows, cols, k):
+    p = _inter(synth.problem(axis, 1, rows, cols, k, seed=14))
+    d = on_device(p)
+    w, win = tcq.trellis_expand(d["codes"], d["scales"], d["lut"], d["g"], with_windows=True)
+    ow, owin = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
+    assert np.array_equal(host_bf16(win), owin) and np.array_equal(host_bf16(w), ow)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_scatter_interleave2_full_size(orc, M):
+    """The pages' k=3 axis-0 production layout at the full scatter geometry."""
+    rows, cols, k = 17408, 5120, 3
+    p = _inter(synth.problem(0, M, rows, cols, k, seed=15))
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128))
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
+    y, a, _, _ = orc.matmul_axis0(p["x"], W)
+    check_close(orc, out, y, a, f"scatter interleave 2 M={M}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_axis1_interleave2(orc, k):
+    rows, cols = 300, 1536
+    p = _inter(synth.problem(1, 8, rows, cols, k, seed=16))
+    d = on_device(p)
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
+    y, a, _ = orc.matmul_axis1(p["x"], W)
+    out = host_bf16(tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"]))
+    check_close(orc, out, y, a, f"prefill interleave 2 k={k}")
+    mv = host_bf16(tcq.trellis_matvec(d["x"][0].contiguous(), d["codes"], d["scales"], d["lut"], d["g"]))
+    check_close(orc, mv[None, :], y[:1], a[:1], f"matvec interleave 2 k={k}")
+
+
+# ----------------------------------------------------------------- wide geometries
+
+def test_prefill_wide_k(orc):
+    """K = 17408 (68 blocks: many stage and ring turns), ragged rows."""
+    rows, cols, k, M = 200, 17408, 3, 16
+    p = synth.problem(1, M, rows, cols, k, seed=17)
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"]))
+    _, y, a = _oracle_axis1(orc, p)
+    check_close(orc, out, y, a, "prefill K=17408")
+    assert tcq.trellis_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_scatter_wide_cols(orc, M):
+    """C = 17408: 17 column ranges, 4 blocks of ranges per split, the last partial."""
+    rows, cols, k = 300, 17408, 4
+    p = synth.problem(0, M, rows, cols, k, seed=18)
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=16))
+    _, y, a, _ = _oracle_axis0(orc, p)
+    check_close(orc, out, y, a, f"scatter C=17408 M={M}")
+
+
 # ----------------------------------------------------------------- glue
 
 def _ulps(a, b):

@@ -50,19 +50,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 trellis_status check_geometry(const trellis_geometry* g, int axis) {
     if (!g) return TRELLIS_ERR_NULL;
-    if (g->bt != 256 || g->L != 12 || g->k < 2 || g->k > 4 || g->interleave != 0)
+    if (g->bt != 256 || g->L != 12 || g->k < 2 || g->k > 4 || (g->interleave != 0 && g->interleave != 2))
         return TRELLIS_ERR_GEOMETRY;
     if (g->axis != 0 && g->axis != 1) return TRELLIS_ERR_GEOMETRY;
     if (g->rows < 1 || g->rows > INT_MAX / 2 || g->cols < 256 || g->cols % 256 != 0 ||
         g->cols > INT_MAX / 2)
         return TRELLIS_ERR_GEOMETRY;
+    if (g->interleave == 2 && (g->cols / 256) % 2 != 0) return TRELLIS_ERR_GEOMETRY;
     if (axis >= 0 && g->axis != axis) return TRELLIS_ERR_SHAPE;
     return TRELLIS_OK;
 }
 
 tcq::Packed packed(const uint32_t* codes, const void* scales, const float* lut,
                    const trellis_geometry* g) {
-    return tcq::Packed{codes, static_cast<const uint16_t*>(scales), lut, g->rows, g->cols, g->k};
+    return tcq::Packed{codes, static_cast<const uint16_t*>(scales), lut, g->rows, g->cols, g->k, g->interleave};
 }
 
 trellis_status launched(cudaError_t e) {

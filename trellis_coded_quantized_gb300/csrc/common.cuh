@@ -152,6 +152,19 @@ __device__ __forceinline__ int next_unit_lane(int lane) {
     return (lane & ~7) | ((lane + 1) & 7);
 }
 
+// Block layout of the codes.  Block b of row r starts at word
+// block_col_base(b) + r * block_row_stride: interleave 0 keeps the blocks of a
+// row contiguous (row stride (cols/256)*wpb); interleave 2 groups blocks in
+// pairs and stores the pair of every row together, base (b/2)*R*2*wpb +
+// (b%2)*wpb and row stride 2*wpb (@mlx-bun/inference 1.0.0,
+// kernels/trellis/vector-expand.ts and scatter.ts, the INTERLEAVE addressing).
+__host__ __device__ __forceinline__ int64_t block_col_base(int64_t b, int64_t rows, int wpb, int interleave) {
+    return interleave == 2 ? (b >> 1) * rows * 2 * wpb + (b & 1) * wpb : b * wpb;
+}
+__host__ __device__ __forceinline__ int64_t block_row_stride(int64_t nblocks, int wpb, int interleave) {
+    return interleave == 2 ? (int64_t)2 * wpb : nblocks * wpb;
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
     return __uint_as_float(h16 << 16);
 }

@@ -13,26 +13,26 @@ namespace {
 template <int K>
 __global__ void __launch_bounds__(256)
 expand_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-              const float* __restrict__ lut, int64_t rows, int64_t units_per_row,
+              const float* __restrict__ lut, int64_t rows, int64_t units_per_row, int interleave,
               uint16_t* __restrict__ w_out, uint16_t* __restrict__ win_out) {
     __shared__ __align__(16) float lut_s[kLutN];
     stage_lut(lut_s, lut);
     __syncthreads();
     const int64_t cols = units_per_row * 32;
-    const int64_t words_per_row = units_per_row * K;
+    constexpr int wpb = kBT * K / 32;
+    const int64_t rs = block_row_stride(units_per_row / kUnitsPerBlock, wpb, interleave);
     const int64_t total = rows * units_per_row;
     for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total;
          id += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = id / units_per_row;
         const int64_t unit = id - r * units_per_row;
         const int u = (int)(unit & 7);
-        const uint32_t* rowp = codes + r * words_per_row;
+        const uint32_t* blk = codes + r * rs + block_col_base(unit >> 3, rows, wpb, interleave);
         uint32_t w[K + 1];
         #pragma unroll
-        for (int j = 0; j < K; ++j) w[j] = __ldg(rowp + unit * K + j);
+        for (int j = 0; j < K; ++j) w[j] = __ldg(blk + u * K + j);
         // neighbour: first word of the next unit of the same block (unit 7 -> unit 0)
-        const int64_t nunit = (u == 7) ? unit - 7 : unit + 1;
-        w[K] = __ldg(rowp + nunit * K);
+        w[K] = __ldg(blk + ((u == 7) ? 0 : (u + 1) * K));
         const float s = bf16_bits_to_float(scales[r]);
         // columns c0 .. c0+31 of this unit; window i is column c0 + 31 - i
         const int64_t c0 = (unit >> 3) * kBT + (224 - 32 * u);
@@ -71,9 +71,9 @@ cudaError_t launch_expand(const Packed& p, uint16_t* w_out, uint16_t* win_out,
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     switch (p.k) {
-        case 2: expand_kernel<2><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, w_out, win_out); break;
-        case 3: expand_kernel<3><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, w_out, win_out); break;
-        case 4: expand_kernel<4><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, w_out, win_out); break;
+        case 2: expand_kernel<2><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, p.interleave, w_out, win_out); break;
+        case 3: expand_kernel<3><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, p.interleave, w_out, win_out); break;
+        case 4: expand_kernel<4><<<(unsigned)blocks, 256, 0, stream>>>(p.codes, p.scales, p.lut, p.rows, units, p.interleave, w_out, win_out); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -14,6 +14,7 @@ struct Packed {              // one packed matrix
     const float* lut;        // f32 [4096]
     int64_t rows, cols;
     int k;                   // bits per symbol
+    int interleave;          // 0: contiguous blocks; 2: blocks paired across rows
 };
 
 cudaError_t launch_expand(const Packed& p, uint16_t* w_out, uint16_t* win_out,

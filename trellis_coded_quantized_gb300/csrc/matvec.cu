@@ -56,7 +56,7 @@ template <int K>
 __global__ void __launch_bounds__(kMvThreads, 1)
 matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
               const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-              int rows, int units, int tg, int ng, uint16_t* __restrict__ out) {
+              int rows, int units, int tg, int ng, int interleave, uint16_t* __restrict__ out) {
     extern __shared__ __align__(16) float smem[];
     float* lut_s = smem;                              // 8-way replicated codebook
     const int wg = tg >> 5;                           // warps per row group
@@ -68,7 +68,7 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const int lane = threadIdx.x & 31;
     const int wig = t >> 5;
     const bool active = t < units;
-    const int64_t wpr = (int64_t)units * K;
+    const int64_t wpr = block_row_stride(units / kUnitsPerBlock, kBT * K / 32, interleave);
     const uint32_t gofs = lut_rep_lane_offset();
 
     // activations of this thread's unit as bf16 pairs: xp[j] holds windows
@@ -96,7 +96,7 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const int r1 = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
     const int per_group = (r1 - r0 + ng - 1) / ng;
     const int src = next_unit_lane(lane);
-    const uint32_t* tp = codes + (int64_t)t * K;
+    const uint32_t* tp = codes + (active ? block_col_base(t >> 3, rows, kBT * K / 32, interleave) + (t & 7) * K : 0);
 
     // two rows in flight ahead of the one being decoded
     uint32_t pa[K], pb[K];
@@ -180,9 +180,9 @@ cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
     }
     if (e != cudaSuccess) return e;
     switch (p.k) {
-        case 2: matvec_kernel<2><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
-        case 3: matvec_kernel<3><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
-        case 4: matvec_kernel<4><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, out); break;
+        case 2: matvec_kernel<2><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
+        case 3: matvec_kernel<3><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
+        case 4: matvec_kernel<4><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

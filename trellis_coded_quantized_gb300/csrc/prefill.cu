@@ -93,7 +93,7 @@ template <int K, int NPAD>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-               int rows, int cols, uint16_t* __restrict__ out, int* __restrict__ status) {
+               int rows, int cols, int interleave, uint16_t* __restrict__ out, int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic on the shared
@@ -185,7 +185,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         // tile cst; each lane's copies arrive on cfull[cst] when they land.
         // Up to kPfCodeStages blocks ahead of the decoders, which release a
         // tile (cempty) as soon as they hold its words in registers.
-        const int64_t wpr = (int64_t)nblocks * wpb;
+        const int64_t wpr = block_row_stride(nblocks, wpb, interleave);
         constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
         const int nchunks = nvalid * cpr;
         for (int b = 0; b < nblocks; ++b) {
@@ -193,7 +193,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
             if (b >= kPfCodeStages &&
                 !tc::mbar_wait(&cempty[cst], (cuse - 1) & 1, abort_flag, kWaitLimitNs)) break;
             const uint32_t ct = tc::smem_addr(cs + cst * Lay::kCodeStage);
-            const uint32_t* src0 = codes + (int64_t)row0 * wpr + (int64_t)b * wpb;
+            const uint32_t* src0 = codes + (int64_t)row0 * wpr + block_col_base(b, rows, wpb, interleave);
             for (int c = lane; c < nchunks; c += 32) {
                 const int r = c / cpr, part = c - (c / cpr) * cpr;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
@@ -290,7 +290,7 @@ cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, 
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((p.rows + kPfRows - 1) / kPfRows);
     prefill_kernel<K, NPAD><<<grid, kPfThreads, smem, stream>>>(x, M, p.codes, p.scales, p.lut,
-                                                                (int)p.rows, (int)p.cols, out, status);
+                                                                (int)p.rows, (int)p.cols, p.interleave, out, status);
     return cudaGetLastError();
 }
 

@@ -36,7 +36,8 @@ template <int K, int MB>
 __global__ void __launch_bounds__(sc_max_warps(MB) * 32, 1)
 scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-               int R, int C, int splits, int rp, int nur, int nurb, float* __restrict__ partial) {
+               int R, int C, int splits, int rp, int nur, int nurb, int interleave,
+               float* __restrict__ partial) {
     constexpr int RW = sc_row_warps(MB);
     extern __shared__ __align__(16) float smem[];
     float* lut_s = smem;                                // 8-way replicated codebook
@@ -56,8 +57,8 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
     const bool active = ur < nur && unit < units;
     const int r0 = s * rp;
     const int r1 = min(R, r0 + rp);
-    const int64_t wpr = (int64_t)units * K;
-    const uint32_t* tp = codes + (int64_t)(active ? unit : 0) * K;
+    const int64_t wpr = block_row_stride(units / kUnitsPerBlock, kBT * K / 32, interleave);
+    const uint32_t* tp = codes + (active ? block_col_base(unit >> 3, R, kBT * K / 32, interleave) + (unit & 7) * K : 0);
     const int src = next_unit_lane(lane);
     const uint32_t gofs = lut_rep_lane_offset();
 
@@ -183,7 +184,7 @@ cudaError_t launch_pass(const Packed& p, const uint16_t* x, int m0, int splits, 
     const unsigned grid = (unsigned)(splits * nblk);
     scatter_kernel<K, MB><<<grid, nurb * RW * 32, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
                                                                   (int)p.rows, (int)p.cols, splits, rp,
-                                                                  nur, nurb, partial);
+                                                                  nur, nurb, p.interleave, partial);
     return cudaGetLastError();
 }
 
