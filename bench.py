@@ -229,6 +229,22 @@ class Workload:
         self.run(self.sets[i % self.nsets])
 
 
+def max_over_ranks(torch, dist, value: float, device) -> float:
+    """The largest `value` over all ranks (the whole job ends with the
+    slowest rank); `value` itself with no process group."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(per_rank_units: float, world: int, seconds: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes
+    per_rank_units in the (max over ranks) time."""
+    return world * per_rank_units / seconds
+
+
 def time_launches(torch, fn, steps, warmup, stream, barrier):
     for i in range(warmup):
         fn(i)
@@ -342,16 +358,13 @@ def run_ours(args):
     wl = Workload(args, torch, tcq, device, l2)
     with ClockSampler(local_rank) as clk:
         total_ms, per = time_launches(torch, wl.step, args.steps, args.warmup, stream, barrier)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, total_ms, device)
     ms = total_ms / args.steps
     sec = total_ms * 1e-3
     if wl.name == "prefill":
-        value, unit = world * wl.flops * args.steps / sec / 1e12, "TFLOP/s"
+        value, unit = job_throughput(wl.flops * args.steps, world, sec) / 1e12, "TFLOP/s"
     else:
-        value, unit = world * wl.packed * args.steps / sec / 1e9, "GB/s"
+        value, unit = job_throughput(wl.packed * args.steps, world, sec) / 1e9, "GB/s"
 
     # roofline of the dominant launch (the only launch of the step, or the
     # scatter with its split reduction)
@@ -383,10 +396,7 @@ def run_ours(args):
 
     e_steps = max(10, min(200, args.steps // 20))
     e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier)
-    if dist:
-        t = torch.tensor([e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(torch, dist, e_ms, device)
     bi = sum(v.numel() * v.element_size() for v in h.values())
     bo = h_out.numel() * 2
     work = wl.flops / 1e12 if wl.name == "prefill" else wl.packed / 1e9

@@ -127,3 +127,16 @@ def test_interleave_two_needs_an_even_block_count(lib):
     assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == GEOM
     g = geometry(1, 256, 512, 2, interleave=2)      # 2 blocks: passes validation up to alignment
     assert lib.trellis_matvec(_p(U), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == ALIGN
+
+
+def test_product_path_never_uses_the_oracle():
+    """The package and its CUDA sources neither import, include, link nor call
+    the oracle (it is test infrastructure only)."""
+    pkg = os.path.join(ROOT, "trellis_coded_quantized_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if not f.endswith((".py", ".cu", ".cuh", ".h")):
+                continue
+            text = open(os.path.join(dirpath, f)).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+            assert "tcq_oracle" not in text and "liboracle" not in text, f
