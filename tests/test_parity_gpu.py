@@ -204,6 +204,38 @@ def test_scatter_partials(orc):
         assert np.all(np.abs(part[:, s, :] - ref[:, s, :]) <= 1e-5 * asum + 1e-30), s
 
 
+@pytest.mark.parametrize("M,k", [(16, 3), (5, 2), (32, 4)])
+def test_scatter_tensor_path_full_size(orc, M, k):
+    """5 or more activation rows take the tensor-core scatter (one pass)."""
+    rows, cols = 17408, 5120
+    p = synth.problem(0, M, rows, cols, k, seed=19)
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128))
+    if M == 16:
+        _, y, a, _ = _oracle_axis0(orc, p)
+        check_close(orc, out, y, a, f"scatter tensor path M={M}")
+    else:
+        rng = np.random.default_rng(M)
+        ms, js = rng.integers(0, M, 3000), rng.integers(0, cols, 3000)
+        y, a = orc.sample(p["x"], p["codes"], rows, cols, k, p["scales"], p["lut"], 0, ms, js)
+        check_close(orc, out[ms, js], y, a, f"scatter tensor path sampled M={M}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_scatter_tensor_path_unit_vectors_exact(orc, k):
+    rows, cols, M = 200, 1024, 8
+    p = synth.problem(0, M, rows, cols, k, seed=20)
+    d = on_device(p)
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
+    rs = [0, 1, 15, 16, 17, 99, 150, 199]
+    e = np.zeros((M, rows), np.uint16)
+    for m, r in enumerate(rs):
+        e[m, r] = ONE
+    out = host_bf16(tcq.trellis_scatter(dev(e), d["codes"], d["scales"], d["lut"], d["g"], splits=7))
+    for m, r in enumerate(rs):
+        assert np.array_equal(out[m], W[r]), (m, r)
+
+
 @pytest.mark.parametrize("k", [2, 3, 4])
 def test_scatter_unit_vectors_exact(orc, k):
     rows, cols = 200, 1024
@@ -272,7 +304,7 @@ def test_prefill_wide_k(orc):
     assert tcq.trellis_device_status() == 0
 
 
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 9])
 def test_scatter_wide_cols(orc, M):
     """C = 17408: 17 column ranges, 4 blocks of ranges per split, the last partial."""
     rows, cols, k = 300, 17408, 4

@@ -27,8 +27,16 @@
 namespace tcq {
 namespace {
 
-constexpr int kMvThreads = 640;
-constexpr int kRB = 16;  // rows per reduction batch (power of two, <= 32)
+// Threads per CTA and rows per reduction batch (a power of two <= 32); the
+// macros let a build try other shapes.
+#ifndef TCQ_MV_THREADS
+#define TCQ_MV_THREADS 640
+#endif
+#ifndef TCQ_MV_RB
+#define TCQ_MV_RB 16
+#endif
+constexpr int kMvThreads = TCQ_MV_THREADS;
+constexpr int kRB = TCQ_MV_RB;
 
 // Butterfly reduce-scatter of a[0..RB) over the 32 lanes: afterwards a[0] of
 // lane l holds the warp sum of row (l >> (5 - log2 RB)) & (RB - 1).
@@ -43,14 +51,22 @@ __device__ __forceinline__ void rs_stage(float* a, int lane, int off) {
     }
 }
 
-__device__ __forceinline__ float reduce_scatter16(float* a, int lane) {
-    rs_stage<8>(a, lane, 16);
-    rs_stage<4>(a, lane, 8);
-    rs_stage<2>(a, lane, 4);
-    rs_stage<1>(a, lane, 2);
-    a[0] += __shfl_xor_sync(0xffffffffu, a[0], 1);
+// Reduce-scatter of RB row sums over the warp: log2(RB) halving stages, then
+// plain butterfly stages; afterwards lane l holds row (l >> (5 - log2 RB)) & (RB-1).
+template <int RB>
+__device__ __forceinline__ float reduce_scatter(float* a, int lane) {
+    static_assert(RB == 8 || RB == 16 || RB == 32, "batch of 8, 16 or 32 rows");
+    if constexpr (RB == 32) rs_stage<16>(a, lane, 16);
+    if constexpr (RB >= 16) rs_stage<8>(a, lane, RB == 32 ? 8 : 16);
+    rs_stage<4>(a, lane, RB == 32 ? 4 : RB == 16 ? 8 : 16);
+    rs_stage<2>(a, lane, RB == 32 ? 2 : RB == 16 ? 4 : 8);
+    rs_stage<1>(a, lane, RB == 32 ? 1 : RB == 16 ? 2 : 4);
+    #pragma unroll
+    for (int off = (RB == 32 ? 0 : RB == 16 ? 1 : 2); off >= 1; off >>= 1)
+        a[0] += __shfl_xor_sync(0xffffffffu, a[0], off);
     return a[0];
 }
+constexpr int kRowShift = kRB == 32 ? 0 : kRB == 16 ? 1 : 2;   // lane -> row of the batch
 
 template <int K>
 __global__ void __launch_bounds__(kMvThreads, 1)
@@ -143,9 +159,9 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
             }
         }
         // rows of this batch: warp reduce-scatter, then sum the warps of the group
-        const float v = reduce_scatter16(acc, lane);
+        const float v = reduce_scatter<kRB>(acc, lane);
         float* rb = red + (size_t)buf * ng * wg * kRB;
-        if ((lane & 1) == 0) rb[((size_t)g * wg + wig) * kRB + ((lane >> 1) & 15)] = v;
+        if ((lane & ((1 << kRowShift) - 1)) == 0) rb[((size_t)g * wg + wig) * kRB + ((lane >> kRowShift) & (kRB - 1))] = v;
         __syncthreads();
         if (t < kRB) {
             const int row = r0 + g + ng * (j0 + t);

@@ -44,6 +44,9 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
     float* red = smem + kLutN * kLutRep;                // [RW-1][nurb][MB][32 cols][32 lanes]
     stage_lut_rep8(lut_s, lut);
     __syncthreads();
+    // let the split reduction be scheduled now (it waits for this grid's
+    // completion before reading anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int nblk = (nur + nurb - 1) / nurb;
     const int s = blockIdx.x / nblk;                    // split
@@ -142,6 +145,9 @@ constexpr int kRdCols = 32;
 __global__ void __launch_bounds__(256)
 split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16_t* __restrict__ out) {
     __shared__ float4 red[kRdGroups][kRdCols / 4];
+    // launched as a programmatic dependent of the scatter: wait until that
+    // grid has completed and its partials are visible (a no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = blockIdx.y;
     const int cq = blockIdx.x * (kRdCols / 4) + (threadIdx.x & 7);   // float4 column index
     const int grp = threadIdx.x >> 3;
@@ -210,20 +216,194 @@ cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, int splits, floa
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Axis-0 scatter for 5..32 activation rows on the tensor cores (mma.sync
+// m16n8k16, bf16 x bf16 -> f32): D[col][m] += W^T[col][r] * X^T[r][m], the
+// output columns are the MMA rows and the input rows of the split are K
+// (the split-K prefill of splitk-prefill.ts computes the same partials with
+// 8x8 simdgroup MMAs).  A warp owns 128-column tiles of its split; lane
+// (g, c) = (lane / 4, lane % 4) owns the 16 consecutive columns 16g..16g+15
+// of the tile, i.e. 16 consecutive windows of each row, and the rows
+// 2c, 2c+1, 2c+8, 2c+9 of every 16-row step.  Its A fragment of m-tile mt
+// takes columns 2mt (MMA row g) and 2mt+1 (row g+8), so the decoded weights
+// go straight from the codebook into fragment registers; B is read from x
+// as K-adjacent pairs.  Each weight is decoded once for all M rows.
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__host__ __device__ constexpr int smma_warps(int nt) { return nt == 1 ? 20 : nt == 2 ? 10 : 8; }
+
+template <int K, int NT>
+__global__ void __launch_bounds__(smma_warps(NT) * 32, 1)
+scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
+                   const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+                   int R, int C, int splits, int rp, int interleave, float* __restrict__ partial) {
+    extern __shared__ __align__(16) float smem[];
+    float* lut_s = smem;                                // 8-way replicated codebook
+    stage_lut_rep8(lut_s, lut);
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    constexpr int wpb = kBT * K / 32;
+    const int s = blockIdx.x;
+    const int r0 = s * rp;
+    const int r1 = min(R, r0 + rp);
+    const int nsteps = (max(r1 - r0, 0) + 15) / 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t gofs = lut_rep_lane_offset();
+    const int64_t rs = block_row_stride(C / kBT, wpb, interleave);
+    const int ntiles = C / 128;
+
+    for (int ct = warp; ct < ntiles; ct += smma_warps(NT)) {
+        const int b = ct >> 1, h = ct & 1;
+        // bits of the 16 windows of this lane: [lo, lo + 15k + 12) of the block
+        const int lo = (240 - 128 * h - 16 * g) * K;
+        const int wl = lo >> 5, sh = lo & 31;
+        const uint32_t* blk = codes + block_col_base(b, R, wpb, interleave);
+        float acc[8][NT][4];
+        #pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+
+        for (int ks = 0; ks < nsteps; ++ks) {
+            // rows 2c, 2c+1, 2c+8, 2c+9 of this 16-row step
+            uint32_t wq[4][3];
+            float sq[4];
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rl = 16 * ks + 2 * c + (q & 1) + 8 * (q >> 1);
+                const int r = r0 + rl;
+                uint32_t w0 = 0u, w1 = 0u, w2 = 0u;
+                sq[q] = 0.f;
+                if (r < r1) {
+                    const uint32_t* rowp = blk + (int64_t)r * rs;
+                    w0 = __ldg(rowp + wl);
+                    w1 = __ldg(rowp + (wl + 1 == wpb ? 0 : wl + 1));
+                    w2 = __ldg(rowp + (wl + 2 >= wpb ? wl + 2 - wpb : wl + 2));
+                    sq[q] = bf16_bits_to_float(__ldg(scales + r));
+                }
+                // bit lo of the block becomes bit 0
+                wq[q][0] = __funnelshift_r(w0, w1, sh);
+                wq[q][1] = __funnelshift_r(w1, w2, sh);
+                wq[q][2] = w2 >> sh;
+            }
+            // B fragments: x[m][r], x[m][r+1] for r = 16ks + 2c (+8)
+            uint32_t bf[NT][2];
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = 8 * nt + g;
+                bf[nt][0] = bf[nt][1] = 0u;
+                if (m < M) {
+                    const uint16_t* xr = x + (int64_t)m * R;
+                    const int ra = r0 + 16 * ks + 2 * c;
+                    const int rb = ra + 8;
+                    // rows past the split or past R read as zero
+                    const uint32_t lo0 = ra < r1 ? xr[ra] : 0u, hi0 = ra + 1 < r1 ? xr[ra + 1] : 0u;
+                    const uint32_t lo1 = rb < r1 ? xr[rb] : 0u, hi1 = rb + 1 < r1 ? xr[rb + 1] : 0u;
+                    bf[nt][0] = lo0 | (hi0 << 16);
+                    bf[nt][1] = lo1 | (hi1 << 16);
+                }
+            }
+            #pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                // column j = 2mt (MMA row g) and j = 2mt+1 (row g+8); window of
+                // column j sits at bit (15 - j) * k of the shifted words
+                float v[4][2];
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[q][0] = lut_at(lut_s, win_off_sh<K, kLutRepShift>(wq[q], 15 - 2 * mt) | gofs);
+                    v[q][1] = lut_at(lut_s, win_off_sh<K, kLutRepShift>(wq[q], 14 - 2 * mt) | gofs);
+                }
+                uint32_t a[4];
+                a[0] = pack_bf16x2(__fmul_rn(v[0][0], sq[0]), __fmul_rn(v[1][0], sq[1]));
+                a[1] = pack_bf16x2(__fmul_rn(v[0][1], sq[0]), __fmul_rn(v[1][1], sq[1]));
+                a[2] = pack_bf16x2(__fmul_rn(v[2][0], sq[2]), __fmul_rn(v[3][0], sq[3]));
+                a[3] = pack_bf16x2(__fmul_rn(v[2][1], sq[2]), __fmul_rn(v[3][1], sq[3]));
+                #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, bf[nt][0], bf[nt][1]);
+            }
+        }
+        // D[row][n]: rows g / g+8 are columns 2mt / 2mt+1, n = 2c, 2c+1 are tokens
+        const int64_t cbase = (int64_t)b * kBT + 128 * h + 16 * g;
+        #pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = 8 * nt + 2 * c;
+                const int64_t col = cbase + 2 * mt;
+                if (m < M)
+                    *reinterpret_cast<float2*>(partial + ((int64_t)m * splits + s) * C + col) =
+                        make_float2(acc[mt][nt][0], acc[mt][nt][2]);
+                if (m + 1 < M)
+                    *reinterpret_cast<float2*>(partial + ((int64_t)(m + 1) * splits + s) * C + col) =
+                        make_float2(acc[mt][nt][1], acc[mt][nt][3]);
+            }
+    }
+}
+
+template <int K, int NT>
+cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
+                          cudaStream_t stream) {
+    const int rp = (int)((p.rows + splits - 1) / splits);
+    const size_t smem = kLutRepBytes;
+    cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    scatter_mma_kernel<K, NT><<<(unsigned)splits, smma_warps(NT) * 32, smem, stream>>>(
+        x, M, p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, partial);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_mma(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
+                       cudaStream_t stream) {
+    if (M <= 8) return launch_mma_nt<K, 1>(p, x, M, splits, partial, stream);
+    if (M <= 16) return launch_mma_nt<K, 2>(p, x, M, splits, partial, stream);
+    return launch_mma_nt<K, 4>(p, x, M, splits, partial, stream);
+}
+
+}  // namespace
+
+
 cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
                            float* partial, uint16_t* out, int sm_count, cudaStream_t stream) {
     (void)sm_count;
     cudaError_t e;
+    // up to 4 activation rows: FMA kernel, each decoded weight feeding every
+    // row; 5 and more: one pass on the tensor cores
     switch (p.k) {
-        case 2: e = launch_k<2>(p, x, M, splits, partial, stream); break;
-        case 3: e = launch_k<3>(p, x, M, splits, partial, stream); break;
-        case 4: e = launch_k<4>(p, x, M, splits, partial, stream); break;
+        case 2: e = M <= 4 ? launch_k<2>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
+        case 3: e = M <= 4 ? launch_k<3>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
+        case 4: e = M <= 4 ? launch_k<4>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     const int C = (int)p.cols;
-    dim3 grid((unsigned)(C / kRdCols), (unsigned)M);
-    split_reduce_kernel<<<grid, 256, 0, stream>>>(partial, splits, C, out);
+    // programmatic dependent launch: the reduction's CTAs are placed while
+    // the last scatter pass still runs and start reading when it completes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(C / kRdCols), (unsigned)M);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(partial), splits, C, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
