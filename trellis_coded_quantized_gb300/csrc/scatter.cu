@@ -22,6 +22,7 @@
 //   - more than 4 activation rows are processed in passes of up to 4.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace tcq {
 namespace {
@@ -252,6 +253,11 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     constexpr int wpb = kBT * K / 32;
+    // per warp: 2 chunks of 16 rows x (4k + 2 used) words of the tile's half
+    // block; the row pitch (20 words for k=3, 4k+4 else) is 4 or 12 mod 16, so
+    // the 4 rows a warp reads at once start 8 banks apart
+    constexpr int kPitchW = K == 3 ? 20 : 4 * K + 4;
+    constexpr int kChunkW = 16 * kPitchW;
     const int s = blockIdx.x;
     const int r0 = s * rp;
     const int r1 = min(R, r0 + rp);
@@ -276,45 +282,81 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 
-        for (int ks = 0; ks < nsteps; ++ks) {
-            // rows 2c, 2c+1, 2c+8, 2c+9 of this 16-row step
-            uint32_t wq[4][3];
-            float sq[4];
+        // The tile's words of a row: the half block [4k(1-h), 4k(1-h) + 4k) and
+        // the two words after it in the block (wrapping to words 0, 1 for
+        // h = 0) -- every window of the 128 columns lies inside them.
+        uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem + kLutN * kLutRep) + warp * 2 * kChunkW;
+        const int span0 = 4 * K * (1 - h);
+        const int ext0 = (span0 + 4 * K) % wpb;
+        const int lw = wl - span0;                      // this lane's first word in a chunk row
+        auto stage = [&](int ks, int buf) {
+            uint32_t* dst = cbuf + buf * kChunkW;
+            for (int idx = lane; idx < 16 * (K + 1); idx += 32) {
+                const int rr = idx / (K + 1), part = idx - rr * (K + 1);
+                const int r = r0 + 16 * ks + rr;
+                if (r >= r1) continue;
+                const uint32_t* rowp = blk + (int64_t)r * rs;
+                const uint32_t sa = tc::smem_addr(dst + rr * kPitchW + 4 * part);
+                if (part < K)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(sa), "l"(rowp + span0 + 4 * part) : "memory");
+                else
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(sa), "l"(rowp + ext0) : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // scales and B operands of a step, one step ahead of their use
+        struct Step { float sq[4]; uint32_t bf[NT][2]; };
+        auto fetch = [&](int ks, Step& st) {
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int rl = 16 * ks + 2 * c + (q & 1) + 8 * (q >> 1);
-                const int r = r0 + rl;
-                uint32_t w0 = 0u, w1 = 0u, w2 = 0u;
-                sq[q] = 0.f;
-                if (r < r1) {
-                    const uint32_t* rowp = blk + (int64_t)r * rs;
-                    w0 = __ldg(rowp + wl);
-                    w1 = __ldg(rowp + (wl + 1 == wpb ? 0 : wl + 1));
-                    w2 = __ldg(rowp + (wl + 2 >= wpb ? wl + 2 - wpb : wl + 2));
-                    sq[q] = bf16_bits_to_float(__ldg(scales + r));
+                const int r = r0 + 16 * ks + 2 * c + (q & 1) + 8 * (q >> 1);
+                st.sq[q] = r < r1 ? bf16_bits_to_float(__ldg(scales + r)) : 0.f;
+            }
+            // B: x[m][r], x[m][r+1] for r = 16ks + 2c (+8); rows past the split read as zero
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = 8 * nt + g;
+                st.bf[nt][0] = st.bf[nt][1] = 0u;
+                if (m < M) {
+                    const uint16_t* xr = x + (int64_t)m * R;
+                    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int ra = r0 + 16 * ks + 2 * c + 8 * hh;
+                        // one 4-byte load when the pair starts on an even element of x
+                        if (((((int64_t)m * R + ra) & 1) == 0) && ra + 1 < r1) {
+                            st.bf[nt][hh] = __ldg(reinterpret_cast<const uint32_t*>(xr + ra));
+                        } else {
+                            const uint32_t lo = ra < r1 ? __ldg(xr + ra) : 0u;
+                            const uint32_t hi = ra + 1 < r1 ? __ldg(xr + ra + 1) : 0u;
+                            st.bf[nt][hh] = lo | (hi << 16);
+                        }
+                    }
                 }
+            }
+        };
+        Step cur, nxt;
+        if (nsteps > 0) { stage(0, 0); fetch(0, cur); }
+        for (int ks = 0; ks < nsteps; ++ks) {
+            if (ks + 1 < nsteps) {
+                stage(ks + 1, (ks + 1) & 1);
+                fetch(ks + 1, nxt);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncwarp();
+            const uint32_t* ch = cbuf + (ks & 1) * kChunkW;
+            uint32_t wq[4][3];
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t* rw = ch + (2 * c + (q & 1) + 8 * (q >> 1)) * kPitchW + lw;
+                const uint32_t w0 = rw[0], w1 = rw[1], w2 = rw[2];
                 // bit lo of the block becomes bit 0
                 wq[q][0] = __funnelshift_r(w0, w1, sh);
                 wq[q][1] = __funnelshift_r(w1, w2, sh);
                 wq[q][2] = w2 >> sh;
             }
-            // B fragments: x[m][r], x[m][r+1] for r = 16ks + 2c (+8)
-            uint32_t bf[NT][2];
-            #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int m = 8 * nt + g;
-                bf[nt][0] = bf[nt][1] = 0u;
-                if (m < M) {
-                    const uint16_t* xr = x + (int64_t)m * R;
-                    const int ra = r0 + 16 * ks + 2 * c;
-                    const int rb = ra + 8;
-                    // rows past the split or past R read as zero
-                    const uint32_t lo0 = ra < r1 ? xr[ra] : 0u, hi0 = ra + 1 < r1 ? xr[ra + 1] : 0u;
-                    const uint32_t lo1 = rb < r1 ? xr[rb] : 0u, hi1 = rb + 1 < r1 ? xr[rb + 1] : 0u;
-                    bf[nt][0] = lo0 | (hi0 << 16);
-                    bf[nt][1] = lo1 | (hi1 << 16);
-                }
-            }
+            const float* sq = cur.sq;
             #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 // column j = 2mt (MMA row g) and j = 2mt+1 (row g+8); window of
@@ -331,8 +373,11 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                 a[2] = pack_bf16x2(__fmul_rn(v[2][0], sq[2]), __fmul_rn(v[3][0], sq[3]));
                 a[3] = pack_bf16x2(__fmul_rn(v[2][1], sq[2]), __fmul_rn(v[3][1], sq[3]));
                 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, bf[nt][0], bf[nt][1]);
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, cur.bf[nt][0], cur.bf[nt][1]);
             }
+            // all lanes are done with this chunk before it is refilled
+            __syncwarp();
+            if (ks + 1 < nsteps) cur = nxt;
         }
         // D[row][n]: rows g / g+8 are columns 2mt / 2mt+1, n = 2c, 2c+1 are tokens
         const int64_t cbase = (int64_t)b * kBT + 128 * h + 16 * g;
@@ -356,7 +401,7 @@ template <int K, int NT>
 cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
                           cudaStream_t stream) {
     const int rp = (int)((p.rows + splits - 1) / splits);
-    const size_t smem = kLutRepBytes;
+    const size_t smem = kLutRepBytes + (size_t)smma_warps(NT) * 2 * 16 * (K == 3 ? 20 : 4 * K + 4) * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
