@@ -186,7 +186,9 @@ class Workload:
             self.splits = getattr(args, "splits", 0) or 128
             self.desc = (f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, "
                          f"{self.splits} splits")
-            self.kernel = "scatter_kernel<3> + split_reduce_kernel"
+            nt = 1 if self.M <= 8 else 2 if self.M <= 16 else 4
+            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 4 else
+                           f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel")
             self.kernel_file = "scatter.cu"
         else:
             raise ValueError(w)

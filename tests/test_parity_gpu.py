@@ -122,6 +122,18 @@ def test_prefill_small(orc, M, k):
     assert tcq.trellis_device_status() == 0
 
 
+def test_prefill_rows_spread_over_sms(orc):
+    """Between 64 and 128 rows per SM each CTA owns ceil(rows / SMs) rows
+    (here 66 on 152 SMs, a ragged last tile); lanes past them decode nothing."""
+    rows, cols, k, M = 10001, 512, 3, 9
+    p = synth.problem(1, M, rows, cols, k, seed=21)
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"]))
+    _, y, a = _oracle_axis1(orc, p)
+    check_close(orc, out, y, a, "prefill spread tiles")
+    assert tcq.trellis_device_status() == 0
+
+
 @pytest.mark.parametrize("M,k", [(32, 4), (5, 2), (16, 3), (8, 4), (32, 2), (32, 3)])
 def test_prefill_full_size(orc, M, k):
     rows, cols = 17408, 5120

@@ -5,7 +5,8 @@
 // kernels/trellis/tiled-prefill.ts): weights decoded to bf16 in the tile,
 // contracted with the bf16 activations, fp32 accumulation, bf16 output.
 //
-// GB300 design (one CTA per 128 weight rows, whole K):
+// GB300 design (one CTA per tile of <= 128 weight rows, whole K; with 64..128
+// rows per SM the rows are spread evenly over all SMs):
 //   - the MMA is D[128 x N] += A[128 x 16] * B[16 x N] with A = decoded
 //     weights (rows of the matrix are MMA rows, "swap AB") held in TENSOR
 //     MEMORY, B = activations in shared memory (K-major, 128-byte swizzle),
@@ -93,7 +94,8 @@ template <int K, int NPAD>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-               int rows, int cols, int interleave, uint16_t* __restrict__ out, int* __restrict__ status) {
+               int rows, int cols, int interleave, int tile_rows, uint16_t* __restrict__ out,
+               int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic on the shared
@@ -137,8 +139,10 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
 
     const int nblocks = cols / kBT;
     constexpr int wpb = Lay::kWpb;
-    const int row0 = blockIdx.x * kPfRows;
-    const int nvalid = min(kPfRows, rows - row0);
+    // this CTA owns tile_rows (<= 128) rows: the MMA always spans 128 lanes,
+    // lanes past the CTA's rows decode nothing and are not stored
+    const int row0 = blockIdx.x * tile_rows;
+    const int nvalid = min(tile_rows, rows - row0);
 
     if (warp < kPfDecWarps) {
         // ------------------------------------------------------------ decoders
@@ -165,13 +169,18 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 #pragma unroll
                 for (int j = 0; j <= K; ++j) w[j] = cw[uu * K + j];   // neighbour is the next unit's first word
                 uint32_t r[16];
-                #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float lo = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - 2 * j) | gofs);
-                    const float hi = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 30 - 2 * j) | gofs);
-                    const uint32_t p2 = pack_bf16x2(__fmul_rn(lo, s), __fmul_rn(hi, s));
-                    r[j] = valid ? p2 : 0u;
+                if (valid) {                                // lanes past the CTA's rows issue no gathers
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float lo = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - 2 * j) | gofs);
+                        const float hi = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 30 - 2 * j) | gofs);
+                        r[j] = pack_bf16x2(__fmul_rn(lo, s), __fmul_rn(hi, s));
+                    }
+                } else {
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = 0u;
                 }
+                __syncwarp();
                 tc::tmem_st16(lane_base + (uint32_t)(stage * 128 + 112 - 16 * u), r);
             }
             tc::tmem_wait_st();
@@ -256,14 +265,15 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const bool ok = tc::mbar_wait(done, 0, abort_flag, kWaitLimitNs);
         __syncwarp();
         tc::tc_fence_after();
-        const int row = row0 + 32 * warp + lane;
+        const int rl = 32 * warp + lane;
+        const int row = row0 + rl;
         const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + kDCol;
         #pragma unroll
         for (int c = 0; c < NPAD; c += 16) {
             uint32_t d[16];
             tc::tmem_ld16(taddr + c, d);
             tc::tmem_wait_ld();
-            if (ok && !*abort_flag && row < rows) {
+            if (ok && !*abort_flag && rl < nvalid) {
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c + j;
@@ -283,33 +293,38 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
 
 template <int K, int NPAD>
 cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, int* status,
-                      cudaStream_t stream) {
+                      int sm_count, cudaStream_t stream) {
     const int smem = PfLayout<K, NPAD>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<K, NPAD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((p.rows + kPfRows - 1) / kPfRows);
+    // Between 64 and 128 rows per SM: spread the rows over all SMs (the decode
+    // is the work, so CTAs with fewer rows finish sooner); else 128-row tiles.
+    int tile_rows = kPfRows;
+    if (sm_count > 0 && p.rows > (int64_t)64 * sm_count && p.rows <= (int64_t)kPfRows * sm_count)
+        tile_rows = (int)((p.rows + sm_count - 1) / sm_count);
+    const unsigned grid = (unsigned)((p.rows + tile_rows - 1) / tile_rows);
     prefill_kernel<K, NPAD><<<grid, kPfThreads, smem, stream>>>(x, M, p.codes, p.scales, p.lut,
-                                                                (int)p.rows, (int)p.cols, p.interleave, out, status);
+                                                                (int)p.rows, (int)p.cols, p.interleave,
+                                                                tile_rows, out, status);
     return cudaGetLastError();
 }
 
 template <int K>
 cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, uint16_t* out, int* status,
-                     cudaStream_t stream) {
-    if (M <= 16) return launch_kn<K, 16>(p, x, M, out, status, stream);
-    return launch_kn<K, 32>(p, x, M, out, status, stream);
+                     int sm_count, cudaStream_t stream) {
+    if (M <= 16) return launch_kn<K, 16>(p, x, M, out, status, sm_count, stream);
+    return launch_kn<K, 32>(p, x, M, out, status, sm_count, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* out,
                            int* status, int sm_count, cudaStream_t stream) {
-    (void)sm_count;
     switch (p.k) {
-        case 2: return launch_k<2>(p, x, M, out, status, stream);
-        case 3: return launch_k<3>(p, x, M, out, status, stream);
-        case 4: return launch_k<4>(p, x, M, out, status, stream);
+        case 2: return launch_k<2>(p, x, M, out, status, sm_count, stream);
+        case 3: return launch_k<3>(p, x, M, out, status, sm_count, stream);
+        case 4: return launch_k<4>(p, x, M, out, status, sm_count, stream);
         default: return cudaErrorInvalidValue;
     }
 }
