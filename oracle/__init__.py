@@ -102,6 +102,9 @@ class Oracle:
         lib.tcq_oracle_matmul_axis1.argtypes = [P, I64, P, I64, I64, P, P, P]
         lib.tcq_oracle_matmul_axis0.argtypes = [P, I64, P, I64, I64, I64, P, P, P, P]
         lib.tcq_oracle_sample.argtypes = [P, I64, P, I64, I64, I, I, I, I, I, P, P, P, P, I64, P, P]
+        lib.tcq_oracle_expand_f32.argtypes = [P, I64, I64, I, I, I, I, P, P, P]
+        lib.tcq_oracle_matmul_axis1_f32w.argtypes = [P, I64, P, I64, I64, P, P, P]
+        lib.tcq_oracle_matmul_axis0_f32w.argtypes = [P, I64, P, I64, I64, P, P, P]
         lib.tcq_oracle_rmsnorm.argtypes = [P, I64, I64, ctypes.c_double, P]
         lib.tcq_oracle_silu_mul.argtypes = [P, P, I64, P]
         self.lib = lib
@@ -200,6 +203,43 @@ class Oracle:
                                    interleave, axis, _ptr(scales), _ptr(lut),
                                    _ptr(ms), _ptr(js), n, _ptr(y), _ptr(a))
         return y, a
+
+    # -- the unrounded contract ----------------------------------------------
+    def expand_f32(self, codes, rows: int, cols: int, k: int, scales, lut, interleave: int = 0,
+                   bt: int = BT, l: int = L):
+        """Weights of the unrounded contract: f32(lut[win] * scale), float32 [rows, cols]."""
+        codes = _c(codes, np.uint32)
+        scales = _c(scales, np.uint16)
+        lut = _c(lut, np.float32)
+        assert codes.size == code_words(rows, cols, k, interleave, bt)
+        w = np.empty((rows, cols), np.float32)
+        self.lib.tcq_oracle_expand_f32(_ptr(codes), rows, cols, bt, k, l, interleave,
+                                       _ptr(scales), _ptr(lut), _ptr(w))
+        return w
+
+    def matmul_axis1_f32w(self, x, w):
+        x = _c(x, np.uint16)
+        w = _c(w, np.float32)
+        M, K = x.shape
+        N, K2 = w.shape
+        assert K == K2
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        out = np.empty((M, N), np.uint16)
+        self.lib.tcq_oracle_matmul_axis1_f32w(_ptr(x), M, _ptr(w), N, K, _ptr(y), _ptr(a), _ptr(out))
+        return y, a, out
+
+    def matmul_axis0_f32w(self, x, w):
+        x = _c(x, np.uint16)
+        w = _c(w, np.float32)
+        M, R = x.shape
+        R2, C = w.shape
+        assert R == R2
+        y = np.empty((M, C), np.float64)
+        a = np.empty((M, C), np.float64)
+        out = np.empty((M, C), np.uint16)
+        self.lib.tcq_oracle_matmul_axis0_f32w(_ptr(x), M, _ptr(w), R, C, _ptr(y), _ptr(a), _ptr(out))
+        return y, a, out
 
     # -- glue of the synthetic MLP stack -------------------------------------
     def rmsnorm(self, x, eps: float = 1e-6):

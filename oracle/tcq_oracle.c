@@ -349,3 +349,70 @@ void tcq_oracle_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n, uint16
         out[i] = tcq_oracle_bf16_from_double(gv / (1.0 + exp(-gv)) * uv);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* the unrounded contract                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A second numerical contract: the weight enters the contraction as the f32
+ * product of codebook value and row scale, with no bf16 rounding in between
+ * (@mlx-bun/inference 1.0.0, kernels/trellis/scatter.ts, the balanced scatter
+ * kernels; kernels/trellis/tiled-prefill.ts, the doc comment of the tiled
+ * prefill, which names the default matvec's unrounded value as a different
+ * contract).
+ *   w32[r][c] = f32( lut[win] * f32(scale[r]) )       (float [rows, cols])
+ */
+void tcq_oracle_expand_f32(const uint32_t* codes, int64_t rows, int64_t cols,
+                           int bt, int k, int L, int interleave,
+                           const uint16_t* scales, const float* lut, float* w_out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        float s = tcq_oracle_bf16_to_float(scales[r]);
+        for (int64_t c = 0; c < cols; c++) {
+            int64_t b = c / bt;
+            int t = (int)(c % bt);
+            const uint32_t* bw = codes + block_base(r, b, rows, cols, bt, k, interleave);
+            uint32_t win = tcq_oracle_window(bw, bt, k, L, t);
+            w_out[r * cols + c] = (float)((double)lut[win] * (double)s);
+        }
+    }
+}
+
+/* Axis 1 on f32 weights: y[m][r] = sum_c x[m][c] w[r][c] (double), a = sum |.|. */
+void tcq_oracle_matmul_axis1_f32w(const uint16_t* x, int64_t M, const float* w,
+                                  int64_t rows, int64_t cols, double* y, double* a, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t m = 0; m < M; m++) {
+            double s = 0.0, sa = 0.0;
+            for (int64_t c = 0; c < cols; c++) {
+                double p = (double)tcq_oracle_bf16_to_float(x[m * cols + c]) * (double)w[r * cols + c];
+                s += p;
+                sa += fabs(p);
+            }
+            if (y) y[m * rows + r] = s;
+            if (a) a[m * rows + r] = sa;
+            if (out) out[m * rows + r] = tcq_oracle_bf16_from_double(s);
+        }
+    }
+}
+
+/* Axis 0 on f32 weights: y[m][c] = sum_r x[m][r] w[r][c] (double), a = sum |.|. */
+void tcq_oracle_matmul_axis0_f32w(const uint16_t* x, int64_t M, const float* w,
+                                  int64_t rows, int64_t cols, double* y, double* a, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < cols; c++) {
+        for (int64_t m = 0; m < M; m++) {
+            double s = 0.0, sa = 0.0;
+            for (int64_t r = 0; r < rows; r++) {
+                double p = (double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[r * cols + c];
+                s += p;
+                sa += fabs(p);
+            }
+            if (y) y[m * cols + c] = s;
+            if (a) a[m * cols + c] = sa;
+            if (out) out[m * cols + c] = tcq_oracle_bf16_from_double(s);
+        }
+    }
+}

@@ -465,11 +465,34 @@ def check_glue(o: _o.Oracle, seed: int = 41):
     assert np.all(np.abs(got - want) <= _o.bf16_ulp(want) * 0.5 + 1e-30)
 
 
+def check_unrounded_contract(o: _o.Oracle, seed: int = 43):
+    """f32 weights: numpy's float32 product of lut[win] and the scale; their
+    bf16 rounding is the rounded contract's weight; both contractions against
+    numpy's float64 matmul."""
+    rng = np.random.default_rng(seed)
+    rows, cols, k, M = 13, 768, 3, 4
+    codes, lut, sc = _random_matrix(rng, rows, cols, k)
+    w32 = o.expand_f32(codes, rows, cols, k, sc, lut)
+    w, win = o.expand(codes, rows, cols, k, sc, lut)
+    want = lut[win.astype(np.int64)] * _o.bf16_to_float(sc)[:, None]      # float32 multiply
+    assert want.dtype == np.float32 and np.array_equal(w32, want)
+    assert np.array_equal(torch_bf16(w32), w)
+    x1 = torch_bf16(rng.standard_normal((M, cols)).astype(np.float32))
+    y, a, _ = o.matmul_axis1_f32w(x1, w32)
+    xf = _o.bf16_to_float(x1).astype(np.float64)
+    assert np.allclose(y, xf @ w32.astype(np.float64).T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(xf) @ np.abs(w32.astype(np.float64)).T, rtol=1e-12, atol=1e-12)
+    x0 = torch_bf16(rng.standard_normal((M, rows)).astype(np.float32))
+    y0, _, _ = o.matmul_axis0_f32w(x0, w32)
+    assert np.allclose(y0, _o.bf16_to_float(x0).astype(np.float64) @ w32.astype(np.float64),
+                       rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_golden_windows, check_windows_random, check_single_bit_probes,
     check_wrap_and_rotation, check_special_patterns, check_bf16_rounding,
     check_weight_rounds_to_f32_first, check_expand_layout,
     check_contraction_vs_numpy, check_unit_vectors_and_bilinear,
     check_reductions, check_lut_readback, check_brute_force_tiny,
-    check_sampled_matches_full, check_glue,
+    check_sampled_matches_full, check_glue, check_unrounded_contract,
 ]

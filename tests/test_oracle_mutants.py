@@ -34,6 +34,10 @@ MUTANTS = {
     "interleave_word_offset": ("+ r * 2 * wpb + (b % 2) * wpb;", "+ r * 2 * wpb + (b % 2);"),
     "rmsnorm_no_mean": ("1.0 / sqrt(ss / (double)D + eps)", "1.0 / sqrt(ss + eps)"),
     "silu_sign": ("gv / (1.0 + exp(-gv)) * uv", "gv / (1.0 + exp(gv)) * uv"),
+    "unrounded_weight_rounded": ("w_out[r * cols + c] = (float)((double)lut[win] * (double)s);",
+                                 "w_out[r * cols + c] = tcq_oracle_bf16_to_float(tcq_oracle_bf16_from_double((double)lut[win] * (double)s));"),
+    "unrounded_axis0_transposed": ("(double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[r * cols + c];",
+                                   "(double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[c * rows + r];"),
 }
 
 
