@@ -104,7 +104,7 @@ class Oracle:
         lib.tcq_oracle_sample.argtypes = [P, I64, P, I64, I64, I, I, I, I, I, P, P, P, P, I64, P, P]
         lib.tcq_oracle_expand_f32.argtypes = [P, I64, I64, I, I, I, I, P, P, P]
         lib.tcq_oracle_matmul_axis1_f32w.argtypes = [P, I64, P, I64, I64, P, P, P]
-        lib.tcq_oracle_matmul_axis0_f32w.argtypes = [P, I64, P, I64, I64, P, P, P]
+        lib.tcq_oracle_matmul_axis0_f32w.argtypes = [P, I64, P, I64, I64, I64, P, P, P, P]
         lib.tcq_oracle_rmsnorm.argtypes = [P, I64, I64, ctypes.c_double, P]
         lib.tcq_oracle_silu_mul.argtypes = [P, P, I64, P]
         self.lib = lib
@@ -229,7 +229,8 @@ class Oracle:
         self.lib.tcq_oracle_matmul_axis1_f32w(_ptr(x), M, _ptr(w), N, K, _ptr(y), _ptr(a), _ptr(out))
         return y, a, out
 
-    def matmul_axis0_f32w(self, x, w):
+    def matmul_axis0_f32w(self, x, w, splits: int = 0):
+        """x bf16 [M, R], w f32 [R, C] -> (y, a, out [M, C], partial f64 [M, splits, C] | None)."""
         x = _c(x, np.uint16)
         w = _c(w, np.float32)
         M, R = x.shape
@@ -238,8 +239,10 @@ class Oracle:
         y = np.empty((M, C), np.float64)
         a = np.empty((M, C), np.float64)
         out = np.empty((M, C), np.uint16)
-        self.lib.tcq_oracle_matmul_axis0_f32w(_ptr(x), M, _ptr(w), R, C, _ptr(y), _ptr(a), _ptr(out))
-        return y, a, out
+        part = np.empty((M, splits, C), np.float64) if splits > 0 else None
+        self.lib.tcq_oracle_matmul_axis0_f32w(_ptr(x), M, _ptr(w), R, C, int(splits),
+                                              _ptr(y), _ptr(a), _ptr(out), _ptr(part))
+        return y, a, out, part
 
     # -- glue of the synthetic MLP stack -------------------------------------
     def rmsnorm(self, x, eps: float = 1e-6):

@@ -398,9 +398,13 @@ void tcq_oracle_matmul_axis1_f32w(const uint16_t* x, int64_t M, const float* w,
     }
 }
 
-/* Axis 0 on f32 weights: y[m][c] = sum_r x[m][r] w[r][c] (double), a = sum |.|. */
+/* Axis 0 on f32 weights: y[m][c] = sum_r x[m][r] w[r][c] (double), a = sum |.|,
+ * and, for splits > 0, the split sums over the same row ranges as the rounded
+ * contract's scatter (rp = ceil(rows / splits)). */
 void tcq_oracle_matmul_axis0_f32w(const uint16_t* x, int64_t M, const float* w,
-                                  int64_t rows, int64_t cols, double* y, double* a, uint16_t* out) {
+                                  int64_t rows, int64_t cols, int64_t splits,
+                                  double* y, double* a, uint16_t* out, double* partial) {
+    int64_t rp = splits > 0 ? (rows + splits - 1) / splits : rows;
 #pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < cols; c++) {
         for (int64_t m = 0; m < M; m++) {
@@ -413,6 +417,15 @@ void tcq_oracle_matmul_axis0_f32w(const uint16_t* x, int64_t M, const float* w,
             if (y) y[m * cols + c] = s;
             if (a) a[m * cols + c] = sa;
             if (out) out[m * cols + c] = tcq_oracle_bf16_from_double(s);
+            if (partial && splits > 0) {
+                for (int64_t sp = 0; sp < splits; sp++) {
+                    int64_t r0 = sp * rp, r1 = r0 + rp < rows ? r0 + rp : rows;
+                    double ps = 0.0;
+                    for (int64_t r = r0; r < r1; r++)
+                        ps += (double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[r * cols + c];
+                    partial[(m * splits + sp) * cols + c] = ps;
+                }
+            }
         }
     }
 }

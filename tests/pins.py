@@ -483,9 +483,14 @@ def check_unrounded_contract(o: _o.Oracle, seed: int = 43):
     assert np.allclose(y, xf @ w32.astype(np.float64).T, rtol=1e-12, atol=1e-12)
     assert np.allclose(a, np.abs(xf) @ np.abs(w32.astype(np.float64)).T, rtol=1e-12, atol=1e-12)
     x0 = torch_bf16(rng.standard_normal((M, rows)).astype(np.float32))
-    y0, _, _ = o.matmul_axis0_f32w(x0, w32)
-    assert np.allclose(y0, _o.bf16_to_float(x0).astype(np.float64) @ w32.astype(np.float64),
-                       rtol=1e-12, atol=1e-12)
+    S = 6                                         # rp = 3: the last split is empty
+    y0, _, _, part = o.matmul_axis0_f32w(x0, w32, S)
+    x0f = _o.bf16_to_float(x0).astype(np.float64)
+    assert np.allclose(y0, x0f @ w32.astype(np.float64), rtol=1e-12, atol=1e-12)
+    for s in range(S):
+        r0, r1 = 3 * s, min(rows, 3 * s + 3)
+        want = x0f[:, r0:r1] @ w32[r0:r1].astype(np.float64) if r0 < r1 else np.zeros((M, cols))
+        assert np.allclose(part[:, s, :], want, rtol=1e-12, atol=1e-12), s
 
 
 ALL_CHECKS = [
