@@ -169,6 +169,9 @@ class Workload:
         self.args, self.torch, self.tcq, self.device = args, torch, tcq, device
         w = args.workload
         self.name = w
+        self.unrounded = bool(getattr(args, "unrounded", False))
+        if self.unrounded and w == "prefill":
+            raise ValueError("the prefill takes the rounded contract only")
         if w in ("decode-matvec", "tiny-matvec"):
             M, K, N, k = (1, 5120, 17408, 4) if w == "decode-matvec" else (1, 512, 256, 2)
             self.M, self.K, self.N, self.k, self.axis = M, K, N, k, 1
@@ -187,7 +190,7 @@ class Workload:
             self.desc = (f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, "
                          f"{self.splits} splits")
             nt = 1 if self.M <= 8 else 2 if self.M <= 16 else 4
-            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 4 else
+            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 4 or self.unrounded else
                            f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel")
             self.kernel_file = "scatter.cu"
         else:
@@ -201,7 +204,10 @@ class Workload:
         codes0, self.scales, self.lut, self.x = dev_problem(torch, p, device)
         self.nsets = max(2, int(np.ceil(4 * l2 / self.packed)) + 1)
         self.sets = xor_sets(torch, codes0, self.nsets, 0x9E3779B9)
-        self.g = tcq.geometry(self.axis, rows, cols, self.k)
+        self.g = tcq.geometry(self.axis, rows, cols, self.k, unrounded=self.unrounded)
+        if self.unrounded:
+            self.desc += ", unrounded contract"
+            self.kernel += " (unrounded)"
         nout = rows if self.axis == 1 else cols
         self.out = torch.empty((self.M, nout), dtype=torch.bfloat16, device=device)
         self.ws = None
@@ -213,7 +219,12 @@ class Workload:
             + self.M * nout * 2
         if w == "scatter":   # the split partials are written and read back once
             self.alg_bytes += 2 * self.M * self.splits * cols * 4
-        self.launches_per_step = 1 if w != "scatter" else 1 + (self.M + 3) // 4
+        # the scatter: FMA passes of up to 4 rows (all M when unrounded), or
+        # one tensor-core pass for 5 and more rows; then the split reduction
+        if w != "scatter":
+            self.launches_per_step = 1
+        else:
+            self.launches_per_step = 1 + ((self.M + 3) // 4 if self.M <= 4 or self.unrounded else 1)
 
     def run(self, codes, x=None, out=None):
         tcq = self.tcq
@@ -278,15 +289,18 @@ def secondary(torch, tcq, device, stream, peaks, l2):
 
     class A:
         pass
-    for w, M, k, S in ([("prefill", M, k, 0) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
-                       [("scatter", 1, 3, 128), ("scatter", 4, 3, 128), ("scatter", 1, 3, 152),
-                        ("scatter", 4, 3, 152), ("tiny-matvec", 1, 2, 0)]):
+    for w, M, k, S, unr in ([("prefill", M, k, 0, False) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
+                            [("scatter", 1, 3, 128, False), ("scatter", 4, 3, 128, False),
+                             ("scatter", 1, 3, 152, False), ("scatter", 4, 3, 152, False),
+                             ("scatter", 16, 3, 128, False), ("tiny-matvec", 1, 2, 0, False),
+                             ("decode-matvec", 1, 4, 0, True), ("scatter", 1, 3, 128, True),
+                             ("scatter", 4, 3, 128, True), ("scatter", 16, 3, 128, True)]):
         a = A()
-        a.workload, a.M, a.k, a.splits = w, M, k, S
+        a.workload, a.M, a.k, a.splits, a.unrounded = w, M, k, S, unr
         wl = Workload(a, torch, tcq, device, l2)
         _, per = time_launches(torch, wl.step, 30, 3, stream, lambda: None)
         t = statistics.median(per) * 1e-3
-        key = f"{w}_M{M}_k{k}" + (f"_s{S}" if w == "scatter" else "")
+        key = f"{w}_M{M}_k{k}" + (f"_s{S}" if w == "scatter" else "") + ("_unrounded" if unr else "")
         rec = {"us": round(t * 1e6, 2), "packed_gbs": round(wl.packed / t / 1e9, 1),
                "tokens_per_s": round(M / t, 1), "frac_of_hbm_alg": round(wl.alg_bytes / t / 1e9 / hbm, 4)}
         if w == "prefill":
@@ -545,6 +559,8 @@ def main():
     ap.add_argument("--M", type=int, default=0, help="activation rows (prefill: 32, scatter: 1)")
     ap.add_argument("--k", type=int, default=0, help="bits per symbol of the prefill (4)")
     ap.add_argument("--splits", type=int, default=0, help="row splits of the scatter (128)")
+    ap.add_argument("--unrounded", action="store_true",
+                    help="the contract without the bf16 rounding of the weight (matvec, scatter)")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -57,6 +57,8 @@ extern "C" {
  *                 (b/2)*rows*2*wpb + r*2*wpb + (b%2)*wpb (vector-expand.ts
  *                 and scatter.ts, INTERLEAVE).  cols must then be a multiple
  *                 of 512.  Same number of words as interleave 0.
+ *   flags: 0, or TRELLIS_FLAG_UNROUNDED.  Any other bit is
+ *                 TRELLIS_ERR_GEOMETRY.
  */
 typedef struct trellis_geometry {
     int32_t axis;
@@ -66,8 +68,22 @@ typedef struct trellis_geometry {
     int64_t rows;
     int64_t cols;
     int32_t interleave;
-    int32_t reserved;
+    int32_t flags;
 } trellis_geometry;
+
+/*
+ * The pages' second numerical contract (scatter.ts, the balanced scatter
+ * kernels; tiled-prefill.ts names the default matvec's unrounded code value
+ * as a different contract): the weight lut[win] * scale[r] enters the
+ * contraction in f32 WITHOUT the bf16 rounding.  The kernels apply the scale
+ * once per row -- to the row sum on axis 1, to the activation x[m][r] on
+ * axis 0 -- which equals the per-weight f32 product up to f32 rounding.
+ * Taken by trellis_matvec, trellis_gate_up_matvec and trellis_scatter (and trellis_scatter_noalloc;
+ * there all M run on the FMA kernel, 4 activation rows per pass).
+ * trellis_prefill and trellis_expand return TRELLIS_ERR_GEOMETRY for it:
+ * their tensor-core operands and their output are the rounded bf16 weight.
+ */
+#define TRELLIS_FLAG_UNROUNDED 1
 
 typedef enum trellis_status {
     TRELLIS_OK = 0,
@@ -91,6 +107,25 @@ typedef enum trellis_status {
 trellis_status trellis_matvec(const void* x, const uint32_t* codes, const void* scales,
                               const float* lut, const trellis_geometry* g,
                               void* out, void* stream);
+
+/*
+ * The gate and up projections of one SwiGLU MLP layer at M = 1 in one
+ * launch, with the SiLU gate applied on the way out (the pages' MLP input
+ * is the RMSNorm output, tiled-prefill.ts; the fused chain is this
+ * library's).  Both matrices have geometry g (axis 1: rows = intermediate
+ * width, cols = hidden width) and share the codebook lut.
+ *   x            bf16 [cols]
+ *   gate_codes, up_codes, gate_scales, up_scales: the two packed matrices
+ *   h_out        bf16 [rows]     h[r] = bf16( silu(gate_r) * up_r ), where
+ *                gate_r = bf16( sum_c x[c] w_gate[r][c] ) and up_r likewise
+ *                (exactly what trellis_matvec and trellis_silu_mul give),
+ *                silu(v) = v / (1 + e^-v) in fp32
+ * Requires g->axis == 1 and cols <= 20480; takes TRELLIS_FLAG_UNROUNDED.
+ * Codes must be 16-byte aligned.
+ */
+trellis_status trellis_gate_up_matvec(const void* x, const uint32_t* gate_codes, const void* gate_scales,
+                                      const uint32_t* up_codes, const void* up_scales, const float* lut,
+                                      const trellis_geometry* g, void* h_out, void* stream);
 
 /*
  * Axis-1 prefill for 1 <= M <= 32 activation rows (tiled-prefill.ts,

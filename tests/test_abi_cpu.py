@@ -129,6 +129,36 @@ def test_interleave_two_needs_an_even_block_count(lib):
     assert lib.trellis_matvec(_p(U), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == ALIGN
 
 
+def test_unrounded_flag_only_where_the_call_takes_it(lib):
+    g1 = geometry(1, 256, 512, 2, unrounded=True)
+    g0 = geometry(0, 512, 256, 3, unrounded=True)
+    # taken: validation goes on to the pointers (misaligned x -> ALIGN)
+    assert lib.trellis_matvec(_p(U), _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    assert lib.trellis_scatter(_p(U), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, _p(A), 1 << 30, _p(A), None) == ALIGN
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 1, 0) == 128 * 256 * 4
+    # refused: the tensor-core prefill and the bf16 expansion
+    assert lib.trellis_prefill(_p(A), 8, _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == GEOM
+    assert lib.trellis_expand(_p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None, None) == GEOM
+    # unknown bits
+    for flags in (2, 3, 1 << 30, -1):
+        g = geometry(1, 256, 512, 2)
+        g.flags = flags
+        assert lib.trellis_matvec(_p(A), _p(A), _p(A), _p(A), ctypes.byref(g), _p(A), None) == GEOM
+
+
+def test_gate_up_validation(lib):
+    g1 = geometry(1, 256, 512, 2)
+    g0 = geometry(0, 256, 512, 2)
+    f = lib.trellis_gate_up_matvec
+    assert f(_p(A), _p(A), _p(A), None, _p(A), _p(A), ctypes.byref(g1), _p(A), None) == NULL
+    assert f(_p(A), _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(g0), _p(A), None) == SHAPE
+    assert f(_p(A), _p(A), _p(A), _p(U), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    wide = geometry(1, 256, 20480 + 256, 4)
+    assert f(_p(A), _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(wide), _p(A), None) == SHAPE
+    gu = geometry(1, 256, 512, 2, unrounded=True)
+    assert f(_p(U), _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(gu), _p(A), None) == ALIGN
+
+
 def test_product_path_never_uses_the_oracle():
     """The package and its CUDA sources neither import, include, link nor call
     the oracle (it is test infrastructure only)."""

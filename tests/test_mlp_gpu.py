@@ -28,11 +28,11 @@ def _ulps(a, b):
     return np.abs(fa - fb) / bf16_ulp(np.maximum(np.abs(fa), np.abs(fb)))
 
 
-def _sampled(orc, x, mat, got, n, rng):
+def _sampled(orc, x, mat, lut, got, n, rng):
     g = mat["g"]
     codes = mat["codes"].cpu().numpy().view(np.uint32)
     scales = mat["scales"].view(__import__("torch").int16).cpu().numpy().view(np.uint16)
-    lut = mat["lut"].cpu().numpy()
+    lut = lut.cpu().numpy()
     M = x.shape[0]
     nout = g.rows if g.axis == 1 else g.cols
     ms = rng.integers(0, M, n)
@@ -56,7 +56,8 @@ def test_stack_stages(orc, stack, M):
         st = {k: host_bf16(v) for k, v in keep[l].items()}
         assert np.all(_ulps(st["n"], orc.rmsnorm(st["x"], 1e-6)) <= 1.0), l
         gate, up, down = stack.layers[l].mats
-        _sampled(orc, st["n"], gate, st["g"], 300, rng)
-        _sampled(orc, st["n"], up, st["u"], 300, rng)
+        _sampled(orc, st["n"], gate, stack.lut, st["g"], 300, rng)
+        _sampled(orc, st["n"], up, stack.lut, st["u"], 300, rng)
+        # M = 1: h comes from the fused gate/up kernel, g and u from trellis_matvec
         assert np.all(_ulps(st["h"], orc.silu_mul(st["g"], st["u"])) <= 1.0), l
-        _sampled(orc, st["h"], down, st["out"], 300, rng)
+        _sampled(orc, st["h"], down, stack.lut, st["out"], 300, rng)

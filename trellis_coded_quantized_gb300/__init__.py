@@ -6,7 +6,9 @@ CUDA tensors in, device pointers out; every step of the computation runs in
 the library's CUDA kernels.  bf16 tensors may be torch.bfloat16 or int16 /
 uint16 holding bf16 bit patterns.
 
-A packed matrix is described by ``geometry(axis, rows, cols, k)``:
+A packed matrix is described by ``geometry(axis, rows, cols, k)``
+(``interleave=2`` for the paired-block layout, ``unrounded=True`` for the
+contract without the bf16 rounding of the weight):
   axis 1: rows are output features, cols input features (x [M, cols] -> [M, rows])
   axis 0: rows are input features, cols output features (x [M, rows] -> [M, cols])
 codes uint32 (int32 storage) [rows, (cols/256)*256*k/32], scales bf16 [rows],
@@ -30,8 +32,12 @@ class TrellisError(RuntimeError):
         super().__init__(f"{where}: {_lib.STATUS.get(status, status)}: {msg}")
 
 
-def geometry(axis: int, rows: int, cols: int, k: int, interleave: int = 0) -> _lib.Geometry:
-    return _lib.Geometry(axis, BT, L, k, rows, cols, interleave, 0)
+FLAG_UNROUNDED = 1   # TRELLIS_FLAG_UNROUNDED: weight lut*scale kept in f32, not rounded to bf16
+
+
+def geometry(axis: int, rows: int, cols: int, k: int, interleave: int = 0,
+             unrounded: bool = False) -> _lib.Geometry:
+    return _lib.Geometry(axis, BT, L, k, rows, cols, interleave, FLAG_UNROUNDED if unrounded else 0)
 
 
 def words_per_row(cols: int, k: int) -> int:
@@ -103,6 +109,23 @@ def trellis_matvec(x, codes, scales, lut, g, out=None, stream=None):
     if out.numel() != g.rows:
         raise ValueError("out must hold rows elements")
     _check(_lib.load().trellis_matvec(xp, c, s, t, ctypes.byref(g), op, _stream(stream)), "trellis_matvec")
+    return out
+
+
+def trellis_gate_up_matvec(x, gate_codes, gate_scales, up_codes, up_scales, lut, g, out=None, stream=None):
+    """M = 1, gate and up projections of one SwiGLU layer (geometry g, one
+    codebook): x bf16 [cols] -> h bf16 [rows], h = bf16(silu(gate) * up)."""
+    cg, sg, t = _packed(gate_codes, gate_scales, lut, g)
+    cu, su, _ = _packed(up_codes, up_scales, lut, g)
+    xp = _dev(x, "x", _bf16_types())
+    if x.numel() != g.cols:
+        raise ValueError("x must hold cols elements")
+    out = _out(out, (g.rows,), x)
+    op = _dev(out, "out", _bf16_types())
+    if out.numel() != g.rows:
+        raise ValueError("out must hold rows elements")
+    _check(_lib.load().trellis_gate_up_matvec(xp, cg, sg, cu, su, t, ctypes.byref(g), op, _stream(stream)),
+           "trellis_gate_up_matvec")
     return out
 
 

@@ -11,7 +11,7 @@ LIB_PATH = os.path.join(HERE, "libtrellis.so")
 
 # the entry points declared in include/trellis.h
 EXPORTS = (
-    "trellis_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_noalloc",
+    "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_noalloc",
     "trellis_scatter_workspace_bytes",
     "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_gather_probe",
     "trellis_device_status", "trellis_strerror",
@@ -26,7 +26,7 @@ STATUS = {
 class Geometry(ctypes.Structure):
     _fields_ = [("axis", ctypes.c_int32), ("bt", ctypes.c_int32), ("L", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
-                ("interleave", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("interleave", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -46,6 +46,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         G = ctypes.POINTER(Geometry)
         sig = {
             "trellis_matvec": ([P, P, P, P, G, P, P], I32),
+            "trellis_gate_up_matvec": ([P, P, P, P, P, P, G, P, P], I32),
             "trellis_prefill": ([P, I32, P, P, P, G, P, P], I32),
             "trellis_scatter": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
             "trellis_scatter_noalloc": ([P, I32, P, P, P, G, I32, P, P], I32),

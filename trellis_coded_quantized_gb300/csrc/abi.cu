@@ -48,8 +48,12 @@ trellis_status current_device(const DeviceFacts** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-trellis_status check_geometry(const trellis_geometry* g, int axis) {
+// axis: the axis the call requires (-1: either); unrounded_ok: whether the
+// call takes TRELLIS_FLAG_UNROUNDED
+trellis_status check_geometry(const trellis_geometry* g, int axis, bool unrounded_ok) {
     if (!g) return TRELLIS_ERR_NULL;
+    if ((g->flags & ~TRELLIS_FLAG_UNROUNDED) != 0) return TRELLIS_ERR_GEOMETRY;
+    if ((g->flags & TRELLIS_FLAG_UNROUNDED) && !unrounded_ok) return TRELLIS_ERR_GEOMETRY;
     if (g->bt != 256 || g->L != 12 || g->k < 2 || g->k > 4 || (g->interleave != 0 && g->interleave != 2))
         return TRELLIS_ERR_GEOMETRY;
     if (g->axis != 0 && g->axis != 1) return TRELLIS_ERR_GEOMETRY;
@@ -63,7 +67,8 @@ trellis_status check_geometry(const trellis_geometry* g, int axis) {
 
 tcq::Packed packed(const uint32_t* codes, const void* scales, const float* lut,
                    const trellis_geometry* g) {
-    return tcq::Packed{codes, static_cast<const uint16_t*>(scales), lut, g->rows, g->cols, g->k, g->interleave};
+    return tcq::Packed{codes, static_cast<const uint16_t*>(scales), lut, g->rows, g->cols, g->k, g->interleave,
+                       (g->flags & TRELLIS_FLAG_UNROUNDED) != 0};
 }
 
 trellis_status launched(cudaError_t e) {
@@ -84,7 +89,7 @@ trellis_status trellis_matvec(const void* x, const uint32_t* codes, const void* 
                               const float* lut, const trellis_geometry* g,
                               void* out, void* stream) {
     if (!x || !codes || !scales || !lut || !g || !out) return TRELLIS_ERR_NULL;
-    trellis_status st = check_geometry(g, 1);
+    trellis_status st = check_geometry(g, 1, true);
     if (st != TRELLIS_OK) return st;
     if (g->cols > tcq::kMatvecMaxCols) return TRELLIS_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(lut)) return TRELLIS_ERR_ALIGN;
@@ -95,11 +100,28 @@ trellis_status trellis_matvec(const void* x, const uint32_t* codes, const void* 
                                        static_cast<cudaStream_t>(stream)));
 }
 
+trellis_status trellis_gate_up_matvec(const void* x, const uint32_t* gate_codes, const void* gate_scales,
+                                     const uint32_t* up_codes, const void* up_scales, const float* lut,
+                                     const trellis_geometry* g, void* h_out, void* stream) {
+    if (!x || !gate_codes || !gate_scales || !up_codes || !up_scales || !lut || !g || !h_out)
+        return TRELLIS_ERR_NULL;
+    trellis_status st = check_geometry(g, 1, true);
+    if (st != TRELLIS_OK) return st;
+    if (g->cols > tcq::kMatvecMaxCols) return TRELLIS_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gate_codes) || !aligned16(up_codes) || !aligned16(lut)) return TRELLIS_ERR_ALIGN;
+    const DeviceFacts* d;
+    if ((st = current_device(&d)) != TRELLIS_OK) return st;
+    return launched(tcq::launch_gate_up_matvec(packed(gate_codes, gate_scales, lut, g), up_codes,
+                                               static_cast<const uint16_t*>(up_scales),
+                                               static_cast<const uint16_t*>(x), static_cast<uint16_t*>(h_out),
+                                               d->sm_count, static_cast<cudaStream_t>(stream)));
+}
+
 trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
                                const void* scales, const float* lut,
                                const trellis_geometry* g, void* out, void* stream) {
     if (!x || !codes || !scales || !lut || !g || !out) return TRELLIS_ERR_NULL;
-    trellis_status st = check_geometry(g, 1);
+    trellis_status st = check_geometry(g, 1, false);
     if (st != TRELLIS_OK) return st;
     if (M < 1 || M > 32) return TRELLIS_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(lut)) return TRELLIS_ERR_ALIGN;
@@ -111,7 +133,7 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
 }
 
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {
-    if (check_geometry(g, -1) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
+    if (check_geometry(g, -1, true) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
     return (size_t)M * (size_t)resolve_splits(splits) * (size_t)g->cols * sizeof(float);
 }
 
@@ -121,7 +143,7 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
                                float* workspace, size_t workspace_bytes,
                                void* out, void* stream) {
     if (!x || !codes || !scales || !lut || !g || !out || !workspace) return TRELLIS_ERR_NULL;
-    trellis_status st = check_geometry(g, 0);
+    trellis_status st = check_geometry(g, 0, true);
     if (st != TRELLIS_OK) return st;
     if (M < 1 || M > 32 || splits < 0 || splits > 1024) return TRELLIS_ERR_SHAPE;
     const int s = resolve_splits(splits);
@@ -140,7 +162,7 @@ trellis_status trellis_expand(const uint32_t* codes, const void* scales, const f
                               const trellis_geometry* g, void* w_out, uint16_t* win_out,
                               void* stream) {
     if (!codes || !scales || !lut || !g || !w_out) return TRELLIS_ERR_NULL;
-    trellis_status st = check_geometry(g, -1);
+    trellis_status st = check_geometry(g, -1, false);
     if (st != TRELLIS_OK) return st;
     if (!aligned16(codes) || !aligned16(lut) || !aligned16(w_out) || (win_out && !aligned16(win_out)))
         return TRELLIS_ERR_ALIGN;
@@ -203,7 +225,7 @@ const char* trellis_strerror(trellis_status status) {
     switch (status) {
         case TRELLIS_OK: return "ok";
         case TRELLIS_ERR_NULL: return "a required pointer is NULL";
-        case TRELLIS_ERR_GEOMETRY: return "unsupported geometry (bt must be 256, L 12, k 2..4, interleave 0, cols a multiple of 256)";
+        case TRELLIS_ERR_GEOMETRY: return "unsupported geometry (bt must be 256, L 12, k 2..4, interleave 0 or 2, cols a multiple of 256 (512 for interleave 2), flags 0 or TRELLIS_FLAG_UNROUNDED where the call takes it)";
         case TRELLIS_ERR_SHAPE: return "size out of range or axis wrong for this entry point";
         case TRELLIS_ERR_ALIGN: return "a buffer is not 16-byte aligned";
         case TRELLIS_ERR_WORKSPACE: return "workspace smaller than trellis_scatter_workspace_bytes()";

@@ -169,4 +169,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
     return __uint_as_float(h16 << 16);
 }
 
+// silu(g) * u in f32, silu(g) = g / (1 + e^-g): the SwiGLU gate of an MLP
+// layer, shared by trellis_silu_mul and the fused gate/up matvec so that the
+// two chains give the same bits.
+__device__ __forceinline__ float silu_mul_f32(float g, float u) {
+    return g / (1.0f + expf(-g)) * u;
+}
+
 }  // namespace tcq

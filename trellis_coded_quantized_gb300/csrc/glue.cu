@@ -35,7 +35,7 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ g, const uint16_t* 
          i += (int64_t)gridDim.x * blockDim.x) {
         const float gv = bf16_bits_to_float(g[i]);
         const float uv = bf16_bits_to_float(u[i]);
-        out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv));
+        out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul_f32(gv, uv)));
     }
 }
 

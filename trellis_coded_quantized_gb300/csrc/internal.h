@@ -15,6 +15,7 @@ struct Packed {              // one packed matrix
     int64_t rows, cols;
     int k;                   // bits per symbol
     int interleave;          // 0: contiguous blocks; 2: blocks paired across rows
+    bool unrounded;          // weight lut*scale not rounded to bf16
 };
 
 cudaError_t launch_expand(const Packed& p, uint16_t* w_out, uint16_t* win_out,
@@ -23,6 +24,11 @@ cudaError_t launch_expand(const Packed& p, uint16_t* w_out, uint16_t* win_out,
 // M = 1, axis 1: out[r] = sum_c x[c] w[r][c]
 cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
                           int sm_count, cudaStream_t stream);
+
+// M = 1, axis 1, the gate and up projections of one SwiGLU layer (same
+// geometry and codebook): h[r] = bf16(silu(bf16(gate_r)) * bf16(up_r))
+cudaError_t launch_gate_up_matvec(const Packed& gate, const uint32_t* up_codes, const uint16_t* up_scales,
+                                  const uint16_t* x, uint16_t* h, int sm_count, cudaStream_t stream);
 
 // axis 1, M in 1..32, tensor cores
 cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* out,

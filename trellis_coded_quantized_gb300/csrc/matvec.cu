@@ -21,6 +21,10 @@
 //   - RB rows are accumulated side by side, then a butterfly reduce-scatter
 //     over the warp (RB shuffles for RB rows) and a sum over the warps of the
 //     group in shared memory produce the RB outputs.
+// The unrounded contract (scatter.ts, balanced scatter kernels; the default
+// matvec per tiled-prefill.ts) drops the bf16 rounding of the weight: the
+// codebook values are contracted with x in f32 and the row's scale
+// multiplies the row sum, one multiply per row instead of one per weight.
 #include "common.cuh"
 #include "internal.h"
 
@@ -68,10 +72,15 @@ __device__ __forceinline__ float reduce_scatter(float* a, int lane) {
 }
 constexpr int kRowShift = kRB == 32 ? 0 : kRB == 16 ? 1 : 2;   // lane -> row of the batch
 
-template <int K>
+// GATEUP: the gate and up projections of a SwiGLU layer in one launch.  The
+// kernel walks 2*rows "virtual" rows, 2r the gate's row r and 2r+1 the up
+// projection's; a CTA owns whole pairs, and the epilogue writes
+// out[r] = bf16(silu(bf16(gate_r)) * bf16(up_r)) instead of the two sums.
+template <int K, bool UNR, bool GATEUP>
 __global__ void __launch_bounds__(kMvThreads, 1)
 matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
-              const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+              const uint16_t* __restrict__ scales, const uint32_t* __restrict__ codes_u,
+              const uint16_t* __restrict__ scales_u, const float* __restrict__ lut,
               int rows, int units, int tg, int ng, int interleave, uint16_t* __restrict__ out) {
     extern __shared__ __align__(16) float smem[];
     float* lut_s = smem;                              // 8-way replicated codebook
@@ -108,22 +117,35 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     }
     __syncthreads();
 
-    const int r0 = (int)((int64_t)rows * blockIdx.x / gridDim.x);
-    const int r1 = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
+    // this CTA's (virtual) rows [r0, r1)
+    const int vm = GATEUP ? 2 : 1;
+    const int r0 = vm * (int)((int64_t)rows * blockIdx.x / gridDim.x);
+    const int r1 = vm * (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
     const int per_group = (r1 - r0 + ng - 1) / ng;
     const int src = next_unit_lane(lane);
-    const uint32_t* tp = codes + (active ? block_col_base(t >> 3, rows, kBT * K / 32, interleave) + (t & 7) * K : 0);
+    const int64_t tofs = active ? block_col_base(t >> 3, rows, kBT * K / 32, interleave) + (t & 7) * K : 0;
+    const uint32_t* tp = codes + tofs;
+    const uint32_t* tpu = GATEUP ? codes_u + tofs : tp;
+    // this thread's words of virtual row v, and the scale of v
+    auto row_words = [&](int v) -> const uint32_t* {
+        if constexpr (GATEUP) return ((v & 1) ? tpu : tp) + (int64_t)(v >> 1) * wpr;
+        else return tp + (int64_t)v * wpr;
+    };
+    auto row_scale = [&](int v) -> float {
+        if constexpr (GATEUP) return bf16_bits_to_float(__ldg(((v & 1) ? scales_u : scales) + (v >> 1)));
+        else return bf16_bits_to_float(__ldg(scales + v));
+    };
 
     // two rows in flight ahead of the one being decoded
     uint32_t pa[K], pb[K];
     {
         const int ra = r0 + g, rb = r0 + g + ng;
-        if (active && ra < r1) load_unit<K>(pa, tp + (int64_t)ra * wpr);
+        if (active && ra < r1) load_unit<K>(pa, row_words(ra));
         else {
             #pragma unroll
             for (int j = 0; j < K; ++j) pa[j] = 0u;
         }
-        if (active && rb < r1) load_unit<K>(pb, tp + (int64_t)rb * wpr);
+        if (active && rb < r1) load_unit<K>(pb, row_words(rb));
         else {
             #pragma unroll
             for (int j = 0; j < K; ++j) pb[j] = 0u;
@@ -140,20 +162,30 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
             #pragma unroll
             for (int j = 0; j < K; ++j) { w[j] = pa[j]; pa[j] = pb[j]; }
             const int rn = row + 2 * ng;
-            if (active && rn < r1) load_unit<K>(pb, tp + (int64_t)rn * wpr);
+            if (active && rn < r1) load_unit<K>(pb, row_words(rn));
             acc[rho] = 0.f;
             if (row < r1) {                              // uniform over the row group
                 w[K] = __shfl_sync(0xffffffffu, w[0], src);
-                const float s = bf16_bits_to_float(__ldg(scales + row));
                 float a0 = 0.f, a1 = 0.f;
-                #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j) | gofs);
-                    const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j + 1) | gofs);
-                    // pair laid out like xp[j]: window 2j high, window 2j+1 low
-                    const uint32_t wp = pack_bf16x2(__fmul_rn(v1, s), __fmul_rn(v0, s));
-                    a0 = fma_bf16_hi(wp, xp[j], a0);
-                    a1 = fma_bf16_lo(wp, xp[j], a1);
+                if constexpr (UNR) {
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j) | gofs);
+                        const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j + 1) | gofs);
+                        a0 = fmaf(v0, __uint_as_float(xp[j] & 0xffff0000u), a0);
+                        a1 = fmaf(v1, __uint_as_float(xp[j] << 16), a1);
+                    }
+                } else {
+                    const float s = row_scale(row);
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j) | gofs);
+                        const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 2 * j + 1) | gofs);
+                        // pair laid out like xp[j]: window 2j high, window 2j+1 low
+                        const uint32_t wp = pack_bf16x2(__fmul_rn(v1, s), __fmul_rn(v0, s));
+                        a0 = fma_bf16_hi(wp, xp[j], a0);
+                        a1 = fma_bf16_lo(wp, xp[j], a1);
+                    }
                 }
                 acc[rho] = a0 + a1;
             }
@@ -163,11 +195,29 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
         float* rb = red + (size_t)buf * ng * wg * kRB;
         if ((lane & ((1 << kRowShift) - 1)) == 0) rb[((size_t)g * wg + wig) * kRB + ((lane >> kRowShift) & (kRB - 1))] = v;
         __syncthreads();
-        if (t < kRB) {
+        if constexpr (GATEUP) {
+            // the batch is the contiguous virtual rows base .. base + ng*kRB - 1
+            // (row g + ng*t of the batch sits at rb[g][.][t]); thread i takes pair i
+            const int base = r0 + ng * j0;
+            const int i = threadIdx.x;
+            if (i < ng * kRB / 2 && base + 2 * i < r1) {
+                float sum[2];
+                #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int o = 2 * i + h, og = o % ng, ot = o / ng;
+                    float a = 0.f;
+                    for (int w = 0; w < wg; ++w) a += rb[((size_t)og * wg + w) * kRB + ot];
+                    if constexpr (UNR) a *= row_scale(base + o);
+                    sum[h] = bf16_bits_to_float(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
+                }
+                out[(base >> 1) + i] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul_f32(sum[0], sum[1])));
+            }
+        } else if (t < kRB) {
             const int row = r0 + g + ng * (j0 + t);
             if (row < r1) {
                 float sum = 0.f;
                 for (int w = 0; w < wg; ++w) sum += rb[((size_t)g * wg + w) * kRB + t];
+                if constexpr (UNR) sum *= row_scale(row);
                 out[row] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
             }
         }
@@ -175,10 +225,21 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     }
 }
 
-}  // namespace
+template <int K, bool UNR, bool GATEUP>
+cudaError_t launch_mv(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x,
+                      uint16_t* out, int grid, int threads, size_t smem, int units, int tg, int ng,
+                      cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(matvec_kernel<K, UNR, GATEUP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    matvec_kernel<K, UNR, GATEUP><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, codes_u, scales_u, p.lut,
+                                                                   (int)p.rows, units, tg, ng, p.interleave, out);
+    return cudaGetLastError();
+}
 
-cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
-                          int sm_count, cudaStream_t stream) {
+template <bool GATEUP>
+cudaError_t launch_any(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x,
+                       uint16_t* out, int sm_count, cudaStream_t stream) {
     const int units = (int)(p.cols / 32);
     const int tg = ((units + 31) / 32) * 32;
     if (tg > kMvThreads) return cudaErrorInvalidValue;
@@ -187,21 +248,27 @@ cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
     int grid = sm_count;
     if ((int64_t)grid > p.rows) grid = (int)p.rows;
     const size_t smem = kLutRepBytes + (size_t)(2 * ng * (tg / 32) * kRB) * sizeof(float);
-    cudaError_t e = cudaSuccess;
-    switch (p.k) {
-        case 2: e = cudaFuncSetAttribute(matvec_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
-        case 3: e = cudaFuncSetAttribute(matvec_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
-        case 4: e = cudaFuncSetAttribute(matvec_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); break;
+    switch (p.k * 2 + (p.unrounded ? 1 : 0)) {
+        case 4: return launch_mv<2, false, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
+        case 5: return launch_mv<2, true, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
+        case 6: return launch_mv<3, false, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
+        case 7: return launch_mv<3, true, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
+        case 8: return launch_mv<4, false, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
+        case 9: return launch_mv<4, true, GATEUP>(p, codes_u, scales_u, x, out, grid, threads, smem, units, tg, ng, stream);
         default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess) return e;
-    switch (p.k) {
-        case 2: matvec_kernel<2><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
-        case 3: matvec_kernel<3><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
-        case 4: matvec_kernel<4><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, p.lut, (int)p.rows, units, tg, ng, p.interleave, out); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_matvec(const Packed& p, const uint16_t* x, uint16_t* out,
+                          int sm_count, cudaStream_t stream) {
+    return launch_any<false>(p, nullptr, nullptr, x, out, sm_count, stream);
+}
+
+cudaError_t launch_gate_up_matvec(const Packed& gate, const uint32_t* up_codes, const uint16_t* up_scales,
+                                  const uint16_t* x, uint16_t* h, int sm_count, cudaStream_t stream) {
+    return launch_any<true>(gate, up_codes, up_scales, x, h, sm_count, stream);
 }
 
 }  // namespace tcq

@@ -19,7 +19,11 @@
 //   - RW warps per column range take interleaved rows of the split and their
 //     partial sums are added in shared memory, in warp order, before the
 //     store of the [MB, 1024] slab of partials;
-//   - more than 4 activation rows are processed in passes of up to 4.
+//   - more than 4 activation rows are processed in passes of up to 4;
+//   - the unrounded contract (scatter.ts, balanced scatter kernels: the f32
+//     product of codebook value and scale, no bf16 rounding) folds the row's
+//     scale into the activations, x[m][r] * scale[r] once per row, and
+//     contracts the codebook values with them in f32.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -33,7 +37,7 @@ namespace {
 __host__ __device__ constexpr int sc_row_warps(int mb) { return mb == 1 ? 4 : 2; }
 __host__ __device__ constexpr int sc_max_warps(int mb) { return mb == 1 ? 20 : 10; }
 
-template <int K, int MB>
+template <int K, int MB, bool UNR>
 __global__ void __launch_bounds__(sc_max_warps(MB) * 32, 1)
 scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const float* __restrict__ lut,
@@ -85,21 +89,37 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
         if (active && rn < r1) load_unit<K>(nxt, tp + (int64_t)rn * wpr);
         w[K] = __shfl_sync(0xffffffffu, w[0], src);
         const float sr = bf16_bits_to_float(__ldg(scales + r));
-        uint32_t xx[MB];                                // x[m][r] in both halves
-        #pragma unroll
-        for (int m = 0; m < MB; ++m) {
-            const uint32_t h = __ldg(x + (int64_t)(m0 + m) * R + r);
-            xx[m] = h | (h << 16);
-        }
-        #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i) | gofs);
-            const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i + 1) | gofs);
-            const uint32_t wp = pack_bf16x2(__fmul_rn(v0, sr), __fmul_rn(v1, sr));
+        if constexpr (UNR) {
+            float xs[MB];                               // x[m][r] * scale[r]
+            #pragma unroll
+            for (int m = 0; m < MB; ++m) xs[m] = bf16_bits_to_float(__ldg(x + (int64_t)(m0 + m) * R + r)) * sr;
+            #pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i) | gofs);
+                const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i + 1) | gofs);
+                #pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    acc[m][i] = fmaf(v0, xs[m], acc[m][i]);
+                    acc[m][i + 1] = fmaf(v1, xs[m], acc[m][i + 1]);
+                }
+            }
+        } else {
+            uint32_t xx[MB];                            // x[m][r] in both halves
             #pragma unroll
             for (int m = 0; m < MB; ++m) {
-                acc[m][i] = fma_bf16_lo(wp, xx[m], acc[m][i]);
-                acc[m][i + 1] = fma_bf16_hi(wp, xx[m], acc[m][i + 1]);
+                const uint32_t h = __ldg(x + (int64_t)(m0 + m) * R + r);
+                xx[m] = h | (h << 16);
+            }
+            #pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float v0 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i) | gofs);
+                const float v1 = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, i + 1) | gofs);
+                const uint32_t wp = pack_bf16x2(__fmul_rn(v0, sr), __fmul_rn(v1, sr));
+                #pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    acc[m][i] = fma_bf16_lo(wp, xx[m], acc[m][i]);
+                    acc[m][i + 1] = fma_bf16_hi(wp, xx[m], acc[m][i + 1]);
+                }
             }
         }
     }
@@ -178,24 +198,24 @@ split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16
     }
 }
 
-template <int K, int MB>
+template <int K, int MB, bool UNR>
 cudaError_t launch_pass(const Packed& p, const uint16_t* x, int m0, int splits, int rp, int nur,
                         float* partial, cudaStream_t stream) {
     constexpr int RW = sc_row_warps(MB);
     const int nurb = nur < sc_max_warps(MB) / RW ? nur : sc_max_warps(MB) / RW;
     const int nblk = (nur + nurb - 1) / nurb;
     const size_t smem = kLutRepBytes + (size_t)(RW - 1) * nurb * MB * 1024 * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(scatter_kernel<K, MB>,
+    cudaError_t e = cudaFuncSetAttribute(scatter_kernel<K, MB, UNR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(splits * nblk);
-    scatter_kernel<K, MB><<<grid, nurb * RW * 32, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
+    scatter_kernel<K, MB, UNR><<<grid, nurb * RW * 32, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
                                                                   (int)p.rows, (int)p.cols, splits, rp,
                                                                   nur, nurb, p.interleave, partial);
     return cudaGetLastError();
 }
 
-template <int K>
+template <int K, bool UNR>
 cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
                      cudaStream_t stream) {
     const int rp = (int)((p.rows + splits - 1) / splits);
@@ -205,10 +225,10 @@ cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, int splits, floa
         const int mb = M - m0 < 4 ? M - m0 : 4;
         cudaError_t e;
         switch (mb) {
-            case 1: e = launch_pass<K, 1>(p, x, m0, splits, rp, nur, partial, stream); break;
-            case 2: e = launch_pass<K, 2>(p, x, m0, splits, rp, nur, partial, stream); break;
-            case 3: e = launch_pass<K, 3>(p, x, m0, splits, rp, nur, partial, stream); break;
-            default: e = launch_pass<K, 4>(p, x, m0, splits, rp, nur, partial, stream); break;
+            case 1: e = launch_pass<K, 1, UNR>(p, x, m0, splits, rp, nur, partial, stream); break;
+            case 2: e = launch_pass<K, 2, UNR>(p, x, m0, splits, rp, nur, partial, stream); break;
+            case 3: e = launch_pass<K, 3, UNR>(p, x, m0, splits, rp, nur, partial, stream); break;
+            default: e = launch_pass<K, 4, UNR>(p, x, m0, splits, rp, nur, partial, stream); break;
         }
         if (e != cudaSuccess) return e;
     }
@@ -426,12 +446,23 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     (void)sm_count;
     cudaError_t e;
     // up to 4 activation rows: FMA kernel, each decoded weight feeding every
-    // row; 5 and more: one pass on the tensor cores
-    switch (p.k) {
-        case 2: e = M <= 4 ? launch_k<2>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
-        case 3: e = M <= 4 ? launch_k<3>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
-        case 4: e = M <= 4 ? launch_k<4>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
-        default: return cudaErrorInvalidValue;
+    // row; 5 and more: one pass on the tensor cores.  The unrounded contract
+    // keeps f32 weights, which the bf16 tensor-core operands cannot carry:
+    // FMA passes of up to 4 rows for every M.
+    if (p.unrounded) {
+        switch (p.k) {
+            case 2: e = launch_k<2, true>(p, x, M, splits, partial, stream); break;
+            case 3: e = launch_k<3, true>(p, x, M, splits, partial, stream); break;
+            case 4: e = launch_k<4, true>(p, x, M, splits, partial, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (p.k) {
+            case 2: e = M <= 4 ? launch_k<2, false>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
+            case 3: e = M <= 4 ? launch_k<3, false>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
+            case 4: e = M <= 4 ? launch_k<4, false>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     if (e != cudaSuccess) return e;
     const int C = (int)p.cols;

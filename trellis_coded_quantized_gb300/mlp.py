@@ -7,8 +7,11 @@ SwiGLU chain is the plain reading of "Qwen's MLP geometry"):
     h = bf16(silu(g) * u)
     x' = down(h)                    axis 0, intermediate -> hidden
 Without a residual.  Layer l, matrix j (0 gate, 1 up, 2 down) is drawn with
-seed 1000*l + j.  M = 1 uses trellis_matvec for gate/up, M >= 2 trellis_prefill;
-down always uses trellis_scatter.  Every step runs in libtrellis kernels.
+seed 1000*l + j; all matrices share one codebook (the pages' codebook is one
+fixed function of the window), drawn with seed CODEBOOK_SEED.  M = 1 runs
+gate, up and silu*up as one trellis_gate_up_matvec, M >= 2 two
+trellis_prefill launches and trellis_silu_mul; down always uses
+trellis_scatter.  Every step runs in libtrellis kernels.
 """
 from __future__ import annotations
 
@@ -19,17 +22,17 @@ from . import synth
 
 HIDDEN = 5120
 INTER = 17408
+CODEBOOK_SEED = 7919
 
 
 class Layer:
-    def __init__(self, l: int, k: int, device, hidden: int, inter: int):
+    def __init__(self, l: int, k: int, device, hidden: int, inter: int, lut):
         import torch
         self.mats = []
         for j, (axis, rows, cols) in enumerate(((1, inter, hidden), (1, inter, hidden), (0, inter, hidden))):
             seed = 1000 * l + j
             codes = synth.codes_torch(seed, rows, cols, k, device)
             scales = torch.from_numpy(synth.scales(seed, rows).view(np.int16)).to(device).view(torch.bfloat16)
-            lut = torch.from_numpy(synth.lut(seed)).to(device)
             self.mats.append({"g": tcq.geometry(axis, rows, cols, k), "codes": codes,
                               "scales": scales, "lut": lut, "seed": seed})
 
@@ -39,7 +42,8 @@ class PackedMLPStack:
                  hidden: int = HIDDEN, inter: int = INTER, splits: int = 128):
         import torch
         self.k, self.hidden, self.inter, self.splits = k, hidden, inter, splits
-        self.layers = [Layer(l, k, device, hidden, inter) for l in range(layers)]
+        self.lut = torch.from_numpy(synth.lut(CODEBOOK_SEED)).to(device)
+        self.layers = [Layer(l, k, device, hidden, inter, self.lut) for l in range(layers)]
         self.device = device
         self.m_max = m_max
         bf = torch.bfloat16
@@ -57,8 +61,10 @@ class PackedMLPStack:
         return len(self.layers) * 3 * self.inter * self.hidden * self.k // 8
 
     def launches_per_pass(self, M: int) -> int:
-        # rmsnorm, gate, up, silu*up, ceil(M/4) scatter passes, the split reduction
-        return len(self.layers) * (4 + (M + 3) // 4 + 1)
+        # rmsnorm; gate+up+silu fused (M = 1) or gate, up, silu*up; the
+        # scatter (ceil(M/4) FMA passes up to 4 rows, one tensor-core pass
+        # from 5 rows); the split reduction
+        return len(self.layers) * (1 + (1 if M == 1 else 3) + ((M + 3) // 4 if M <= 4 else 1) + 1)
 
     def layer(self, l: int, x, out, keep=None):
         """One layer on x [M, hidden] into out [M, hidden]."""
@@ -67,13 +73,16 @@ class PackedMLPStack:
         n, g, u, h = self.n[:M], self.gate[:M], self.up[:M], self.h[:M]
         tcq.trellis_rmsnorm(x, 1e-6, out=n)
         if M == 1:
-            tcq.trellis_matvec(n[0], gate["codes"], gate["scales"], gate["lut"], gate["g"], out=g[0])
-            tcq.trellis_matvec(n[0], up["codes"], up["scales"], up["lut"], up["g"], out=u[0])
+            tcq.trellis_gate_up_matvec(n[0], gate["codes"], gate["scales"], up["codes"], up["scales"], self.lut,
+                                       gate["g"], out=h[0])
+            if keep is not None:        # the two projections on their own, for stage checks
+                tcq.trellis_matvec(n[0], gate["codes"], gate["scales"], self.lut, gate["g"], out=g[0])
+                tcq.trellis_matvec(n[0], up["codes"], up["scales"], self.lut, up["g"], out=u[0])
         else:
-            tcq.trellis_prefill(n, gate["codes"], gate["scales"], gate["lut"], gate["g"], out=g)
-            tcq.trellis_prefill(n, up["codes"], up["scales"], up["lut"], up["g"], out=u)
-        tcq.trellis_silu_mul(g, u, out=h)
-        tcq.trellis_scatter(h, down["codes"], down["scales"], down["lut"], down["g"], splits=self.splits,
+            tcq.trellis_prefill(n, gate["codes"], gate["scales"], self.lut, gate["g"], out=g)
+            tcq.trellis_prefill(n, up["codes"], up["scales"], self.lut, up["g"], out=u)
+            tcq.trellis_silu_mul(g, u, out=h)
+        tcq.trellis_scatter(h, down["codes"], down["scales"], self.lut, down["g"], splits=self.splits,
                             workspace=self.ws, out=out)
         if keep is not None:
             keep.append({"x": x.clone(), "n": n.clone(), "g": g.clone(), "u": u.clone(), "h": h.clone(),
