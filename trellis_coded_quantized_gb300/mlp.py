@@ -11,7 +11,8 @@ seed 1000*l + j; all matrices share one codebook (the pages' codebook is one
 fixed function of the window), drawn with seed CODEBOOK_SEED.  M = 1 runs
 gate, up and silu*up as one trellis_gate_up_matvec, M >= 2 two
 trellis_prefill launches and trellis_silu_mul; down always uses
-trellis_scatter.  Every step runs in libtrellis kernels.
+trellis_scatter, with one split per SM by default.  Every step runs in
+libtrellis kernels.
 """
 from __future__ import annotations
 
@@ -39,8 +40,10 @@ class Layer:
 
 class PackedMLPStack:
     def __init__(self, layers: int = 40, k: int = 3, device="cuda", m_max: int = 16,
-                 hidden: int = HIDDEN, inter: int = INTER, splits: int = 128):
+                 hidden: int = HIDDEN, inter: int = INTER, splits: int | None = None):
         import torch
+        if splits is None:      # one split per SM: every SM gets a share of the down projection
+            splits = torch.cuda.get_device_properties(device).multi_processor_count
         self.k, self.hidden, self.inter, self.splits = k, hidden, inter, splits
         self.lut = torch.from_numpy(synth.lut(CODEBOOK_SEED)).to(device)
         self.layers = [Layer(l, k, device, hidden, inter, self.lut) for l in range(layers)]
