@@ -66,14 +66,53 @@ constexpr int kLutRep = 8;
 constexpr int kLutRepShift = 5;
 constexpr size_t kLutRepBytes = (size_t)kLutN * kLutRep * sizeof(float);
 
+// All of a thread's codebook loads are issued before its first store, so the
+// staging costs one global-memory latency per 8 entries instead of one per
+// entry (a CTA of 512..1024 threads stages the table in one round).
 __device__ __forceinline__ void stage_lut_rep8(float* lut_s, const float* __restrict__ lut) {
     float4* dst = reinterpret_cast<float4*>(lut_s);
-    for (int e = threadIdx.x; e < kLutN; e += blockDim.x) {
-        const float v = __ldg(lut + e);
-        const float4 q = make_float4(v, v, v, v);
-        dst[2 * e] = q;
-        dst[2 * e + 1] = q;
+    for (int base = threadIdx.x; base < kLutN; base += 8 * blockDim.x) {
+        float v[8];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = base + i * blockDim.x;
+            v[i] = e < kLutN ? __ldg(lut + e) : 0.f;
+        }
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = base + i * blockDim.x;
+            if (e < kLutN) {
+                const float4 q = make_float4(v[i], v[i], v[i], v[i]);
+                dst[2 * e] = q;
+                dst[2 * e + 1] = q;
+            }
+        }
     }
+}
+
+// Programmatic dependent launch.  A kernel launched with
+// launch_pdl() may be placed on the GPU while the previous kernel of its
+// stream still runs; pdl_wait() blocks until that kernel has completed and
+// its writes are visible, so it comes before the first global-memory access.
+// pdl_release() lets the next such kernel be placed.  Both are no-ops for a
+// kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // Byte offset of this lane's copy inside an entry of the replicated codebook.

@@ -10,6 +10,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 rmsnorm_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* __restrict__ out) {
     __shared__ float part[8];
+    pdl_wait();
+    pdl_release();
     const uint16_t* xr = x + (int64_t)blockIdx.x * D;
     uint16_t* orow = out + (int64_t)blockIdx.x * D;
     float ss = 0.f;
@@ -31,6 +33,8 @@ rmsnorm_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* _
 
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                 int64_t n, uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_release();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float gv = bf16_bits_to_float(g[i]);
@@ -74,7 +78,8 @@ gather_probe_kernel(const float* __restrict__ lut, int iters, float* __restrict_
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t M, int64_t D, float eps,
                            uint16_t* out, cudaStream_t stream) {
-    rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(x, D, eps, out);
+    const cudaError_t e = launch_pdl(rmsnorm_kernel, dim3((unsigned)M), dim3(256), 0, stream, x, D, eps, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -83,7 +88,8 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
-    silu_mul_kernel<<<(unsigned)blocks, 256, 0, stream>>>(g, u, n, out);
+    const cudaError_t e = launch_pdl(silu_mul_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, g, u, n, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -83,6 +83,8 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
               const uint16_t* __restrict__ scales_u, const float* __restrict__ lut,
               int rows, int units, int tg, int ng, int interleave, uint16_t* __restrict__ out) {
     extern __shared__ __align__(16) float smem[];
+    pdl_release();
+    pdl_wait();
     float* lut_s = smem;                              // 8-way replicated codebook
     const int wg = tg >> 5;                           // warps per row group
     float* red = smem + kLutN * kLutRep;              // [2][ng][wg][kRB]
@@ -232,8 +234,9 @@ cudaError_t launch_mv(const Packed& p, const uint32_t* codes_u, const uint16_t* 
     cudaError_t e = cudaFuncSetAttribute(matvec_kernel<K, UNR, GATEUP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    matvec_kernel<K, UNR, GATEUP><<<grid, threads, smem, stream>>>(x, p.codes, p.scales, codes_u, scales_u, p.lut,
-                                                                   (int)p.rows, units, tg, ng, p.interleave, out);
+    e = launch_pdl(matvec_kernel<K, UNR, GATEUP>, dim3(grid), dim3(threads), smem, stream, x, p.codes, p.scales,
+                   codes_u, scales_u, p.lut, (int)p.rows, units, tg, ng, p.interleave, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

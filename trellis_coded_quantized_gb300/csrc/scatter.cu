@@ -45,13 +45,14 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
                float* __restrict__ partial) {
     constexpr int RW = sc_row_warps(MB);
     extern __shared__ __align__(16) float smem[];
+    pdl_wait();                                         // x, and the partials the last reduction read
     float* lut_s = smem;                                // 8-way replicated codebook
     float* red = smem + kLutN * kLutRep;                // [RW-1][nurb][MB][32 cols][32 lanes]
     stage_lut_rep8(lut_s, lut);
     __syncthreads();
     // let the split reduction be scheduled now (it waits for this grid's
     // completion before reading anything)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release();
 
     const int nblk = (nur + nurb - 1) / nurb;
     const int s = blockIdx.x / nblk;                    // split
@@ -168,7 +169,8 @@ split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16
     __shared__ float4 red[kRdGroups][kRdCols / 4];
     // launched as a programmatic dependent of the scatter: wait until that
     // grid has completed and its partials are visible (a no-op otherwise)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
+    pdl_release();
     const int m = blockIdx.y;
     const int cq = blockIdx.x * (kRdCols / 4) + (threadIdx.x & 7);   // float4 column index
     const int grp = threadIdx.x >> 3;
@@ -209,9 +211,9 @@ cudaError_t launch_pass(const Packed& p, const uint16_t* x, int m0, int splits, 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(splits * nblk);
-    scatter_kernel<K, MB, UNR><<<grid, nurb * RW * 32, smem, stream>>>(x, m0, p.codes, p.scales, p.lut,
-                                                                  (int)p.rows, (int)p.cols, splits, rp,
-                                                                  nur, nurb, p.interleave, partial);
+    e = launch_pdl(scatter_kernel<K, MB, UNR>, dim3(grid), dim3(nurb * RW * 32), smem, stream, x, m0, p.codes,
+                   p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, nur, nurb, p.interleave, partial);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -267,10 +269,11 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                    const uint16_t* __restrict__ scales, const float* __restrict__ lut,
                    int R, int C, int splits, int rp, int interleave, float* __restrict__ partial) {
     extern __shared__ __align__(16) float smem[];
+    pdl_wait();
     float* lut_s = smem;                                // 8-way replicated codebook
     stage_lut_rep8(lut_s, lut);
     __syncthreads();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release();
 
     constexpr int wpb = kBT * K / 32;
     // per warp: 2 chunks of 16 rows x (4k + 2 used) words of the tile's half
@@ -425,8 +428,9 @@ cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits,
     cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    scatter_mma_kernel<K, NT><<<(unsigned)splits, smma_warps(NT) * 32, smem, stream>>>(
-        x, M, p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, partial);
+    e = launch_pdl(scatter_mma_kernel<K, NT>, dim3((unsigned)splits), dim3(smma_warps(NT) * 32), smem, stream, x, M,
+                   p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, partial);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -468,17 +472,8 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     const int C = (int)p.cols;
     // programmatic dependent launch: the reduction's CTAs are placed while
     // the last scatter pass still runs and start reading when it completes
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(C / kRdCols), (unsigned)M);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(partial), splits, C, out);
+    e = launch_pdl(split_reduce_kernel, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0, stream,
+                   static_cast<const float*>(partial), splits, C, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -11,7 +11,7 @@ seed 1000*l + j; all matrices share one codebook (the pages' codebook is one
 fixed function of the window), drawn with seed CODEBOOK_SEED.  M = 1 runs
 gate, up and silu*up as one trellis_gate_up_matvec, M >= 2 two
 trellis_prefill launches and trellis_silu_mul; down always uses
-trellis_scatter, with one split per SM by default.  Every step runs in
+trellis_scatter (split count by M, see splits_for).  Every step runs in
 libtrellis kernels.
 """
 from __future__ import annotations
@@ -42,8 +42,7 @@ class PackedMLPStack:
     def __init__(self, layers: int = 40, k: int = 3, device="cuda", m_max: int = 16,
                  hidden: int = HIDDEN, inter: int = INTER, splits: int | None = None):
         import torch
-        if splits is None:      # one split per SM: every SM gets a share of the down projection
-            splits = torch.cuda.get_device_properties(device).multi_processor_count
+        self.sm_count = torch.cuda.get_device_properties(device).multi_processor_count
         self.k, self.hidden, self.inter, self.splits = k, hidden, inter, splits
         self.lut = torch.from_numpy(synth.lut(CODEBOOK_SEED)).to(device)
         self.layers = [Layer(l, k, device, hidden, inter, self.lut) for l in range(layers)]
@@ -56,8 +55,22 @@ class PackedMLPStack:
         self.h = torch.empty((m_max, inter), dtype=bf, device=device)
         self.xs = [torch.empty((m_max, hidden), dtype=bf, device=device) for _ in range(2)]
         g0 = self.layers[0].mats[2]["g"]
-        self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(g0, m_max, splits) // 4,
+        most = max(self.splits_for(M) for M in range(1, m_max + 1))
+        self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(g0, m_max, most) // 4,
                               dtype=torch.float32, device=device)
+
+    def splits_for(self, M: int) -> int:
+        """Row splits of the down projection: the constructor's, else one per
+        SM for the FMA scatter (M <= 4), and for the tensor-core scatter the
+        fewest splits whose row ranges are whole 16-row MMA steps at the
+        SM-limited step count (17408 rows on 152 SMs: 136 splits of 128)."""
+        if self.splits:
+            return self.splits
+        if M <= 4:
+            return self.sm_count
+        steps = -(-self.inter // 16)
+        per = -(-steps // self.sm_count)
+        return -(-self.inter // (16 * per))
 
     @property
     def packed_bytes(self) -> int:
@@ -85,7 +98,7 @@ class PackedMLPStack:
             tcq.trellis_prefill(n, gate["codes"], gate["scales"], self.lut, gate["g"], out=g)
             tcq.trellis_prefill(n, up["codes"], up["scales"], self.lut, up["g"], out=u)
             tcq.trellis_silu_mul(g, u, out=h)
-        tcq.trellis_scatter(h, down["codes"], down["scales"], self.lut, down["g"], splits=self.splits,
+        tcq.trellis_scatter(h, down["codes"], down["scales"], self.lut, down["g"], splits=self.splits_for(M),
                             workspace=self.ws, out=out)
         if keep is not None:
             keep.append({"x": x.clone(), "n": n.clone(), "g": g.clone(), "u": u.clone(), "h": h.clone(),
