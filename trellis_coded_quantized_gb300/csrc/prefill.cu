@@ -13,10 +13,10 @@
 //     D = fp32 accumulator in tensor memory; N = 16 or 32 (M padded);
 //   - 1 code-loader warp: per 256-column block it copies the block of all
 //     128 rows in coalesced 16-byte cp.async chunks (completion tracked on
-//     an mbarrier) into one of 3 shared-memory tiles whose row pitch is 16
+//     an mbarrier) into one of 2 shared-memory tiles whose row pitch is 16
 //     bytes more than a block, so 8 consecutive rows fall in 8 different
 //     bank groups; the decoders release a tile as soon as they hold its
-//     words, so the loads run up to 3 blocks ahead;
+//     words, so the loads run up to 2 blocks ahead;
 //   - 1 activation-loader warp copies the activation tile of each block
 //     (cp.async, zero-filled rows M..N-1) into the swizzled layout;
 //   - 16 decoder warps: warp w owns tensor-memory lane quarter w % 4 (32
@@ -28,8 +28,8 @@
 //     into the A stage: decoded weights never touch shared memory;
 //   - 1 MMA warp: one thread waits for a stage, issues 16 tcgen05.mma
 //     (K = 16 each) and commits to the stage's "empty" barrier;
-//   - 2 stages (A: 2 x 128 tensor-memory columns, B: 2 x N x 512 bytes,
-//     codes: 2 x 128 rows), mbarriers with bounded waits; after the last
+//   - 3 stages (A: 3 x 128 tensor-memory columns beside the accumulator,
+//     B: 3 x N x 512 bytes), mbarriers with bounded waits; after the last
 //     block the accumulator is read back with tcgen05.ld by the lane-quarter
 //     warps and stored as bf16.
 // The K order of a block is the natural column order on both operands.
@@ -47,10 +47,25 @@ constexpr int kPfMmaWarp = kPfDecWarps;
 constexpr int kPfLoadWarp = kPfDecWarps + 1;      // activation tiles
 constexpr int kPfCodeWarp = kPfDecWarps + 2;      // code tiles
 constexpr int kPfThreads = (kPfDecWarps + 3) * 32;
-constexpr int kPfCodeStages = 3;
+// Stages of the A operand (tensor memory) and the activations, and of the
+// code tiles; the macros let a build try other depths.
+// Three A stages let the decoders run two blocks ahead of the MMA (M=32:
+// 2 us faster at k=2 and 3 on GB300); two code tiles keep the k=4, N=32
+// layout within 227 KB of shared memory.
+#ifndef TCQ_PF_ASTAGES
+#define TCQ_PF_ASTAGES 3
+#endif
+#ifndef TCQ_PF_CSTAGES
+#define TCQ_PF_CSTAGES 2
+#endif
+constexpr int kPfAStages = TCQ_PF_ASTAGES;
+constexpr int kPfCodeStages = TCQ_PF_CSTAGES;
+static_assert(kPfAStages == 2 || kPfAStages == 3, "2 or 3 A stages fit beside the accumulator");
 constexpr int kPfRows = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator columns [256, 256 + N)
+// tensor-memory column of A stage st: [0, 128), [128, 256), [384, 512)
+__host__ __device__ constexpr uint32_t a_col(int st) { return st < 2 ? (uint32_t)st * 128u : 384u; }
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 template <int K, int NPAD>
@@ -59,7 +74,7 @@ struct PfLayout {
     static constexpr int kPitch = kWpb * 4 + 16;           // bytes per row of a code tile
     static constexpr int kXStage = NPAD * kBT * 2;         // bytes of one activation stage
     static constexpr int kXChunk = NPAD * 128;             // one 64-column K chunk
-    static constexpr int kCodeOff = 2 * kXStage;
+    static constexpr int kCodeOff = kPfAStages * kXStage;
     static constexpr int kCodeStage = kPfRows * kPitch;
     static constexpr int kLutOff = kCodeOff + kPfCodeStages * kCodeStage;
     static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
@@ -106,17 +121,17 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     uint8_t* cs = base + Lay::kCodeOff;
     float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);   // decoders + activations
-    uint64_t* empty = full + 2;                                           // MMA done with a stage
-    uint64_t* cfull = full + 4;                                           // code tile landed [3]
-    uint64_t* cempty = full + 7;                                          // code tile read [3]
-    uint64_t* done = full + 10;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 11);
+    uint64_t* empty = full + kPfAStages;                                  // MMA done with a stage
+    uint64_t* cfull = empty + kPfAStages;                                 // code tile landed
+    uint64_t* cempty = cfull + kPfCodeStages;                             // code tile read
+    uint64_t* done = cempty + kPfCodeStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     stage_lut_rep8(lut_s, lut);
     if (threadIdx.x == 0) {
-        for (int st = 0; st < 2; ++st) {
+        for (int st = 0; st < kPfAStages; ++st) {
             tc::mbar_init(&full[st], kPfDecWarps * 32 + 32);
             tc::mbar_init(&empty[st], 1);
         }
@@ -153,13 +168,13 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t gofs = lut_rep_lane_offset();
         for (int b = 0; b < nblocks; ++b) {
-            const int stage = b & 1;
+            const int stage = b % kPfAStages, use = b / kPfAStages;
             const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
             if (!tc::mbar_wait(&cfull[cst], cuse & 1, abort_flag, kWaitLimitNs)) break;
             uint32_t cw[kPfUnits * K + 1];
             read_quarter<K>(cw, cs + cst * Lay::kCodeStage + rl * Lay::kPitch, part);
             tc::mbar_arrive(&cempty[cst]);                 // the code tile may be refilled
-            if (b >= 2 && !tc::mbar_wait(&empty[stage], ((b >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) break;
+            if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
             __syncwarp();
             tc::tc_fence_after();
             #pragma unroll
@@ -181,7 +196,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                     for (int j = 0; j < 16; ++j) r[j] = 0u;
                 }
                 __syncwarp();
-                tc::tmem_st16(lane_base + (uint32_t)(stage * 128 + 112 - 16 * u), r);
+                tc::tmem_st16(lane_base + a_col(stage) + (uint32_t)(112 - 16 * u), r);
             }
             tc::tmem_wait_st();
             tc::tc_fence_before();
@@ -219,8 +234,8 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         // into the async proxy before arriving on full[stage].
         const uint32_t xs_base = tc::smem_addr(xs);
         for (int b = 0; b < nblocks; ++b) {
-            const int stage = b & 1;
-            if (b >= 2 && !tc::mbar_wait(&empty[stage], ((b >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) break;
+            const int stage = b % kPfAStages, use = b / kPfAStages;
+            if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
             __syncwarp();
             const uint32_t st = xs_base + stage * Lay::kXStage;
             #pragma unroll 8
@@ -243,12 +258,12 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, NPAD);
             const uint32_t xs_base = tc::smem_addr(xs);
             for (int b = 0; b < nblocks; ++b) {
-                const int stage = b & 1;
-                if (!tc::mbar_wait(&full[stage], (b >> 1) & 1, abort_flag, kWaitLimitNs)) break;
+                const int stage = b % kPfAStages;
+                if (!tc::mbar_wait(&full[stage], (b / kPfAStages) & 1, abort_flag, kWaitLimitNs)) break;
                 tc::tc_fence_after();
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const uint32_t a = tmem + (uint32_t)(stage * 128 + 8 * j);
+                    const uint32_t a = tmem + a_col(stage) + (uint32_t)(8 * j);
                     const uint64_t bd = tc::sdesc_sw128(
                         xs_base + stage * Lay::kXStage + (j >> 2) * Lay::kXChunk + (j & 3) * 32, 1024);
                     tc::mma_ts(tmem + kDCol, a, bd, idesc, (b | j) != 0 ? 1u : 0u);
