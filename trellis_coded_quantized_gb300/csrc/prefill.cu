@@ -113,6 +113,10 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
+    // a programmatic dependent of the previous kernel: nothing is read,
+    // written or allocated (tensor memory) before that kernel has completed
+    pdl_wait();
+    pdl_release();
     // 1024-byte aligned base, derived by pointer arithmetic on the shared
     // array (an integer round trip would lose the shared address space and
     // turn every table gather into a generic load)
@@ -319,9 +323,9 @@ cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, 
     if (sm_count > 0 && p.rows > (int64_t)64 * sm_count && p.rows <= (int64_t)kPfRows * sm_count)
         tile_rows = (int)((p.rows + sm_count - 1) / sm_count);
     const unsigned grid = (unsigned)((p.rows + tile_rows - 1) / tile_rows);
-    prefill_kernel<K, NPAD><<<grid, kPfThreads, smem, stream>>>(x, M, p.codes, p.scales, p.lut,
-                                                                (int)p.rows, (int)p.cols, p.interleave,
-                                                                tile_rows, out, status);
+    e = launch_pdl(prefill_kernel<K, NPAD>, dim3(grid), dim3(kPfThreads), (size_t)smem, stream, x, M, p.codes,
+                   p.scales, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
