@@ -424,13 +424,20 @@ def run_ours(args):
         h_out.copy_(d_out, non_blocking=True)
 
     e_steps = max(10, min(200, args.steps // 20))
-    e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier)
+    e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier, per_launch=False)
     e_ms = max_over_ranks(torch, dist, e_ms, device)
+    # the end-to-end result must be the device path's result, bit for bit
+    torch.cuda.synchronize()
+    ref_out = torch.empty_like(d_out)
+    wl.run(wl.sets[0] if hasattr(wl, "sets") else d["codes"], out=ref_out.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    e2e_same = bool(torch.equal(h_out, ref_out.cpu()))
     bi = sum(v.numel() * v.element_size() for v in h.values())
     bo = h_out.numel() * 2
     work = wl.flops / 1e12 if wl.name == "prefill" else wl.packed / 1e9
     e2e = {"value": round(world * work * e_steps / (e_ms * 1e-3), 3), "unit": unit,
-           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e_ms / e_steps, 4)}
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e_ms / e_steps, 4),
+           "matches_device_path": e2e_same}
 
     extras = None
     if rank == 0 and not args.no_extras:
