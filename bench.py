@@ -160,6 +160,32 @@ def dev_problem(torch, p, device):
             torch.from_numpy(p["x"].view(np.int16)).to(device).view(torch.bfloat16))
 
 
+def workload_config(args) -> dict:
+    """The workload's shape and its JSON `config` (shared by both arms)."""
+    w = args.workload
+    unrounded = bool(getattr(args, "unrounded", False))
+    splits = None
+    if w in ("decode-matvec", "tiny-matvec"):
+        M, K, N, k, axis = (1, 5120, 17408, 4, 1) if w == "decode-matvec" else (1, 512, 256, 2, 1)
+        desc = (f"decode matvec axis-1: M=1, K={K}, N={N}, k={k}, BT=256, L=12" if w == "decode-matvec"
+                else f"tiny axis-1 matvec: M=1, K={K}, N={N}, k={k}, BT=256, L=12, seed 0")
+    elif w == "prefill":
+        M, K, N, k, axis = args.M or 32, 5120, 17408, args.k or 4, 1
+        desc = f"tiled prefill axis-1: M={M}, K=5120, N=17408, k={k}, BT=256, L=12"
+    elif w == "scatter":
+        M, K, N, k, axis = args.M or 1, 17408, 5120, 3, 0
+        splits = getattr(args, "splits", 0) or 128
+        desc = f"axis-0 split-K scatter: M={M}, R=17408, C=5120, k=3, BT=256, L=12, {splits} splits"
+    else:
+        raise ValueError(w)
+    if unrounded:
+        desc += ", unrounded contract"
+    rows, cols = (N, K) if axis == 1 else (K, N)
+    return {"name": w, "M": M, "K": K, "N": N, "k": k, "axis": axis, "rows": rows, "cols": cols,
+            "splits": splits, "unrounded": unrounded, "desc": desc,
+            "config": {"workload": desc, "M": M, "K_in": K, "N_out": N, "k": k, "BT": 256, "L": 12, "axis": axis}}
+
+
 class Workload:
     """One configuration: step(i) runs one pass of the hot path on weight set
     i mod nsets; the step's launches are timed for the roofline."""
@@ -169,26 +195,21 @@ class Workload:
         self.args, self.torch, self.tcq, self.device = args, torch, tcq, device
         w = args.workload
         self.name = w
-        self.unrounded = bool(getattr(args, "unrounded", False))
+        cf = workload_config(args)
+        self.cfg = cf
+        self.unrounded = cf["unrounded"]
         if self.unrounded and w == "prefill":
             raise ValueError("the prefill takes the rounded contract only")
+        self.M, self.K, self.N, self.k, self.axis = cf["M"], cf["K"], cf["N"], cf["k"], cf["axis"]
+        self.desc = cf["desc"]
         if w in ("decode-matvec", "tiny-matvec"):
-            M, K, N, k = (1, 5120, 17408, 4) if w == "decode-matvec" else (1, 512, 256, 2)
-            self.M, self.K, self.N, self.k, self.axis = M, K, N, k, 1
-            self.desc = (f"decode matvec axis-1: M=1, K={K}, N={N}, k={k}, BT=256, L=12" if w == "decode-matvec"
-                         else f"tiny axis-1 matvec: M=1, K={K}, N={N}, k={k}, BT=256, L=12, seed 0")
-            self.kernel = f"matvec_kernel<{k}>"
+            self.kernel = f"matvec_kernel<{self.k}>"
             self.kernel_file = "matvec.cu"
         elif w == "prefill":
-            self.M, self.K, self.N, self.k, self.axis = args.M or 32, 5120, 17408, args.k or 4, 1
-            self.desc = f"tiled prefill axis-1: M={self.M}, K=5120, N=17408, k={self.k}, BT=256, L=12"
             self.kernel = f"prefill_kernel<{self.k},{16 if self.M <= 16 else 32}>"
             self.kernel_file = "prefill.cu"
         elif w == "scatter":
-            self.M, self.K, self.N, self.k, self.axis = args.M or 1, 17408, 5120, 3, 0
-            self.splits = getattr(args, "splits", 0) or 128
-            self.desc = (f"axis-0 split-K scatter: M={self.M}, R=17408, C=5120, k=3, BT=256, L=12, "
-                         f"{self.splits} splits")
+            self.splits = cf["splits"]
             nt = 1 if self.M <= 8 else 2 if self.M <= 16 else 4
             self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 4 or self.unrounded else
                            f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel")
@@ -206,7 +227,6 @@ class Workload:
         self.sets = xor_sets(torch, codes0, self.nsets, 0x9E3779B9)
         self.g = tcq.geometry(self.axis, rows, cols, self.k, unrounded=self.unrounded)
         if self.unrounded:
-            self.desc += ", unrounded contract"
             self.kernel += " (unrounded)"
         nout = rows if self.axis == 1 else cols
         self.out = torch.empty((self.M, nout), dtype=torch.bfloat16, device=device)
@@ -457,9 +477,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded SplitMix64 codes, N(0,1) codebook and activations, U[0.01,0.03] scales)",
-            "config": {"workload": wl.desc, "M": wl.M, "K_in": wl.cols if wl.axis == 1 else wl.rows,
-                       "N_out": wl.rows if wl.axis == 1 else wl.cols, "k": wl.k, "BT": 256, "L": 12,
-                       "axis": wl.axis, "weight_sets": wl.nsets,
+            "config": {**wl.cfg["config"], "weight_sets": wl.nsets,
                        "l2": f"inputs larger than L2: {wl.nsets} rotating weight sets "
                              f"({wl.nsets * wl.packed / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"independent problem per GPU x{world}"},
@@ -483,6 +501,13 @@ def oracle_pass(orc, wl, rows):
     p = wl.p
     codes = p["codes"][:rows]
     t0 = time.perf_counter()
+    if getattr(wl, "unrounded", False):        # the unrounded contract: f32 weights
+        W = orc.expand_f32(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
+        if wl.axis == 1:
+            orc.matmul_axis1_f32w(p["x"], W)
+        else:
+            orc.matmul_axis0_f32w(p["x"][:, :rows], W)
+        return time.perf_counter() - t0
     W, _ = orc.expand(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
     if wl.axis == 1:
         orc.matmul_axis1(p["x"], W)
@@ -516,21 +541,16 @@ class _HostWorkload:
 
     def __init__(self, args):
         from trellis_coded_quantized_gb300 import synth
-        w = args.workload
-        self.name = w
-        if w == "decode-matvec":
-            self.M, rows, cols, self.k, self.axis = 1, 17408, 5120, 4, 1
-        elif w == "tiny-matvec":
-            self.M, rows, cols, self.k, self.axis = 1, 256, 512, 2, 1
-        elif w == "prefill":
-            self.M, rows, cols, self.k, self.axis = args.M or 32, 17408, 5120, args.k or 4, 1
-        else:
-            self.M, rows, cols, self.k, self.axis = args.M or 1, 17408, 5120, 3, 0
+        cf = workload_config(args)
+        self.cfg = cf
+        self.name = cf["name"]
+        self.M, self.k, self.axis, self.unrounded = cf["M"], cf["k"], cf["axis"], cf["unrounded"]
+        rows, cols = cf["rows"], cf["cols"]
         self.rows, self.cols = rows, cols
         self.packed = rows * cols * self.k // 8
         self.flops = 2.0 * self.M * rows * cols
         self.p = synth.problem(self.axis, self.M, rows, cols, self.k, seed=0)
-        self.desc = f"{w}: M={self.M}, rows={rows}, cols={cols}, k={self.k}, axis {self.axis}"
+        self.desc = cf["desc"]
 
 
 def run_reference(args):
@@ -560,7 +580,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (the same seeded inputs)",
-        "config": {"workload": wl.desc, "sample": f"{rows} of {wl.rows} rows per step"},
+        "config": {**wl.cfg["config"], "sample": f"{rows} of {wl.rows} rows per step"},
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": orc.max_threads(), "kind": "oracle",
                          "sample": f"{rows} of the {wl.rows} matrix rows per step (expand + double contraction)"},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
