@@ -430,26 +430,45 @@ def run_ours(args):
          "scales": torch.from_numpy(wl.p["scales"].view(np.int16)).pin_memory(),
          "lut": torch.from_numpy(wl.p["lut"]).pin_memory(),
          "x": torch.from_numpy(wl.p["x"].view(np.int16)).pin_memory()}
-    h_out = torch.empty(tuple(wl.out.shape), dtype=torch.int16).pin_memory()
-    d = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h.items()}
-    d_out = torch.empty(tuple(wl.out.shape), dtype=torch.int16, device=device)
+    # Two sets of device buffers: the copies of step i+1 run on a side stream
+    # while the kernel of step i runs; every step still copies all of its
+    # inputs in and its result out inside the timed region.
+    h_outs = [torch.empty(tuple(wl.out.shape), dtype=torch.int16).pin_memory() for _ in range(2)]
+    ds = [{k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h.items()} for _ in range(2)]
+    d_outs = [torch.empty(tuple(wl.out.shape), dtype=torch.int16, device=device) for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device)
+    landed = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    last = {"b": 0}
+    e_warm = 3
 
     def e2e_step(i):
-        for k in d:
-            d[k].copy_(h[k], non_blocking=True)
+        b = i % 2
+        d = ds[b]
+        if i in (0, e_warm):                     # the first warm-up and the first timed step start
+            copy_stream.wait_stream(stream)      # after everything before them (the start event)
+        copy_stream.wait_event(done[b])          # step i-2 no longer reads these buffers
+        with torch.cuda.stream(copy_stream):
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+            landed[b].record(copy_stream)
+        stream.wait_event(landed[b])
         sc, lt = wl.scales, wl.lut
         wl.scales, wl.lut = d["scales"].view(torch.bfloat16), d["lut"]
-        wl.run(d["codes"], x=d["x"].view(torch.bfloat16), out=d_out.view(torch.bfloat16))
+        wl.run(d["codes"], x=d["x"].view(torch.bfloat16), out=d_outs[b].view(torch.bfloat16))
         wl.scales, wl.lut = sc, lt
-        h_out.copy_(d_out, non_blocking=True)
+        h_outs[b].copy_(d_outs[b], non_blocking=True)
+        done[b].record(stream)
+        last["b"] = b
 
     e_steps = max(10, min(200, args.steps // 20))
-    e_ms, _ = time_launches(torch, e2e_step, e_steps, 3, stream, barrier, per_launch=False)
+    e_ms, _ = time_launches(torch, e2e_step, e_steps, e_warm, stream, barrier, per_launch=False)
+    h_out, d_out = h_outs[last["b"]], d_outs[last["b"]]
     e_ms = max_over_ranks(torch, dist, e_ms, device)
     # the end-to-end result must be the device path's result, bit for bit
     torch.cuda.synchronize()
     ref_out = torch.empty_like(d_out)
-    wl.run(wl.sets[0] if hasattr(wl, "sets") else d["codes"], out=ref_out.view(torch.bfloat16))
+    wl.run(wl.sets[0], out=ref_out.view(torch.bfloat16))
     torch.cuda.synchronize()
     e2e_same = bool(torch.equal(h_out, ref_out.cpu()))
     bi = sum(v.numel() * v.element_size() for v in h.values())
