@@ -279,7 +279,7 @@ def test_expand_interleave2_bit_exact(orc, axis, rows, cols, k):
     assert np.array_equal(host_bf16(win), owin) and np.array_equal(host_bf16(w), ow)
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 16])
 def test_scatter_interleave2_full_size(orc, M):
     """The pages' k=3 axis-0 production layout at the full scatter geometry."""
     rows, cols, k = 17408, 5120, 3
@@ -289,6 +289,17 @@ def test_scatter_interleave2_full_size(orc, M):
     W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
     y, a, _, _ = orc.matmul_axis0(p["x"], W)
     check_close(orc, out, y, a, f"scatter interleave 2 M={M}")
+
+
+@pytest.mark.parametrize("rows,cols,k,M,splits", [(301, 1024, 2, 5, 7), (300, 2048, 4, 32, 13), (129, 512, 3, 9, 1024)])
+def test_scatter_tensor_path_interleave2(orc, rows, cols, k, M, splits):
+    """The tensor-core scatter on the interleave-2 layout, odd split sizes."""
+    p = _inter(synth.problem(0, M, rows, cols, k, seed=17))
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=splits))
+    W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
+    y, a, _, _ = orc.matmul_axis0(p["x"], W)
+    check_close(orc, out, y, a, f"tensor scatter interleave 2 {rows}x{cols} k={k} M={M} S={splits}")
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])
