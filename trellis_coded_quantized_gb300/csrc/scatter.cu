@@ -357,9 +357,11 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                 }
             }
         };
-        Step cur, nxt;
-        if (nsteps > 0) { stage(0, 0); fetch(0, cur); }
-        for (int ks = 0; ks < nsteps; ++ks) {
+        // the step loop unrolled by two: the operands of step ks+1 are
+        // fetched into the other Step instead of being copied at the end of
+        // the step (M=16: 2%, M=32: 5% faster on GB300)
+        Step sa, sb;
+        auto one_step = [&](int ks, Step& cur, Step& nxt) {
             if (ks + 1 < nsteps) {
                 stage(ks + 1, (ks + 1) & 1);
                 fetch(ks + 1, nxt);
@@ -400,7 +402,11 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
             }
             // all lanes are done with this chunk before it is refilled
             __syncwarp();
-            if (ks + 1 < nsteps) cur = nxt;
+        };
+        if (nsteps > 0) { stage(0, 0); fetch(0, sa); }
+        for (int ks = 0; ks < nsteps; ks += 2) {
+            one_step(ks, sa, sb);
+            if (ks + 1 < nsteps) one_step(ks + 1, sb, sa);
         }
         // D[row][n]: rows g / g+8 are columns 2mt / 2mt+1, n = 2c, 2c+1 are tokens
         const int64_t cbase = (int64_t)b * kBT + 128 * h + 16 * g;
