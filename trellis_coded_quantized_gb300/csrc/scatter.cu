@@ -263,17 +263,21 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 
 __host__ __device__ constexpr int smma_warps(int nt) { return nt == 1 ? 20 : nt == 2 ? 10 : 8; }
 
-template <int K, int NT>
+// XS: the split's activations (bf16 [NT*8][xpitch], rows past the split and
+// activation rows past M zero) and scales (f32 [rp16]) are staged in shared
+// memory once per CTA, so the B operands and scales of a step are
+// conflict-free shared loads (xpitch/2 words = 4 mod 32: lanes (g, c) hit
+// banks 4g + c) instead of global loads that touch 8 lines each.
+template <int K, int NT, bool XS>
 __global__ void __launch_bounds__(smma_warps(NT) * 32, 1)
 scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, const float* __restrict__ lut,
-                   int R, int C, int splits, int rp, int interleave, float* __restrict__ partial) {
+                   int R, int C, int splits, int rp, int interleave, int xpitch, int rp16,
+                   float* __restrict__ partial) {
     extern __shared__ __align__(16) float smem[];
     pdl_wait();
     float* lut_s = smem;                                // 8-way replicated codebook
     stage_lut_rep8(lut_s, lut);
-    __syncthreads();
-    pdl_release();
 
     constexpr int wpb = kBT * K / 32;
     // per warp: 2 chunks of 16 rows x (4k + 2 used) words of the tile's half
@@ -285,6 +289,27 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
     const int r0 = s * rp;
     const int r1 = min(R, r0 + rp);
     const int nsteps = (max(r1 - r0, 0) + 15) / 16;
+    uint32_t* xs32 = reinterpret_cast<uint32_t*>(smem + kLutN * kLutRep) + smma_warps(NT) * 2 * kChunkW;
+    float* ss = reinterpret_cast<float*>(xs32 + NT * 8 * (xpitch >> 1));
+    if constexpr (XS) {
+        const int nr = max(r1 - r0, 0);
+        const int hp = xpitch >> 1;
+        for (int i = threadIdx.x; i < NT * 8 * hp; i += blockDim.x) {
+            const int m = i / hp, rr = 2 * (i - m * hp);
+            uint32_t v = 0u;
+            if (m < M) {
+                const uint16_t* xr = x + (int64_t)m * R + r0;
+                const uint32_t lo16 = rr < nr ? __ldg(xr + rr) : 0u;
+                const uint32_t hi16 = rr + 1 < nr ? __ldg(xr + rr + 1) : 0u;
+                v = lo16 | (hi16 << 16);
+            }
+            xs32[i] = v;
+        }
+        for (int i = threadIdx.x; i < rp16; i += blockDim.x)
+            ss[i] = i < nr ? bf16_bits_to_float(__ldg(scales + r0 + i)) : 0.f;
+    }
+    __syncthreads();
+    pdl_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const uint32_t gofs = lut_rep_lane_offset();
@@ -330,6 +355,16 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
         // scales and B operands of a step, one step ahead of their use
         struct Step { float sq[4]; uint32_t bf[NT][2]; };
         auto fetch = [&](int ks, Step& st) {
+            if constexpr (XS) {
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) st.sq[q] = ss[16 * ks + 2 * c + (q & 1) + 8 * (q >> 1)];
+                #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        st.bf[nt][hh] = xs32[(8 * nt + g) * (xpitch >> 1) + 8 * ks + c + 4 * hh];
+                return;
+            }
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int r = r0 + 16 * ks + 2 * c + (q & 1) + 8 * (q >> 1);
@@ -426,18 +461,35 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
     }
 }
 
+template <int K, int NT, bool XS>
+cudaError_t launch_mma_xs(const Packed& p, const uint16_t* x, int M, int splits, int rp, int xpitch, int rp16,
+                          size_t smem, float* partial, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT, XS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(scatter_mma_kernel<K, NT, XS>, dim3((unsigned)splits), dim3(smma_warps(NT) * 32), smem, stream,
+                   x, M, p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, xpitch, rp16,
+                   partial);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// Activations and scales of a split go to shared memory when they take at
+// most this many bytes (row splits of up to ~600 rows at M = 32); longer
+// splits read them from global memory.
+constexpr size_t kXsBudget = 40960;
+
 template <int K, int NT>
 cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
                           cudaStream_t stream) {
     const int rp = (int)((p.rows + splits - 1) / splits);
-    const size_t smem = kLutRepBytes + (size_t)smma_warps(NT) * 2 * 16 * (K == 3 ? 20 : 4 * K + 4) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(scatter_mma_kernel<K, NT>, dim3((unsigned)splits), dim3(smma_warps(NT) * 32), smem, stream, x, M,
-                   p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, partial);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    const int rp16 = (rp + 15) / 16 * 16;
+    const int xpitch = rp16 + (((8 - rp16) % 64) + 64) % 64;     // xpitch / 2 words = 4 mod 32
+    const size_t xs_bytes = (size_t)NT * 8 * xpitch * 2 + (size_t)rp16 * 4;
+    const size_t base = kLutRepBytes + (size_t)smma_warps(NT) * 2 * 16 * (K == 3 ? 20 : 4 * K + 4) * sizeof(uint32_t);
+    if (xs_bytes <= kXsBudget)
+        return launch_mma_xs<K, NT, true>(p, x, M, splits, rp, xpitch, rp16, base + xs_bytes, partial, stream);
+    return launch_mma_xs<K, NT, false>(p, x, M, splits, rp, 0, rp16, base, partial, stream);
 }
 
 template <int K>
