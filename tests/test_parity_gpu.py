@@ -219,7 +219,7 @@ def test_scatter_partials(orc):
 
 @pytest.mark.parametrize("M,k", [(16, 3), (5, 2), (32, 4)])
 def test_scatter_tensor_path_full_size(orc, M, k):
-    """5 or more activation rows take the tensor-core scatter (one pass)."""
+    """3 or more activation rows take the tensor-core scatter (one pass)."""
     rows, cols = 17408, 5120
     p = synth.problem(0, M, rows, cols, k, seed=19)
     d = on_device(p)

@@ -240,7 +240,7 @@ cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, int splits, floa
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Axis-0 scatter for 5..32 activation rows on the tensor cores (mma.sync
+// Axis-0 scatter for 3..32 activation rows on the tensor cores (mma.sync
 // m16n8k16, bf16 x bf16 -> f32): D[col][m] += W^T[col][r] * X^T[r][m], the
 // output columns are the MMA rows and the input rows of the split are K
 // (the split-K prefill of splitk-prefill.ts computes the same partials with
@@ -503,12 +503,20 @@ cudaError_t launch_mma(const Packed& p, const uint16_t* x, int M, int splits, fl
 }  // namespace
 
 
+// Fewest activation rows that take the tensor-core scatter (GB300, 17408 x
+// 5120, k=3, back to back: M=2 FMA 47.7 / tensor 54.6 us, M=3 61.4 / 56.0,
+// M=4 65.9 / 57.6).
+#ifndef TCQ_MMA_MIN_ROWS
+#define TCQ_MMA_MIN_ROWS 3
+#endif
+constexpr int kMmaMinRows = TCQ_MMA_MIN_ROWS;
+
 cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
                            float* partial, uint16_t* out, int sm_count, cudaStream_t stream) {
     (void)sm_count;
     cudaError_t e;
-    // up to 4 activation rows: FMA kernel, each decoded weight feeding every
-    // row; 5 and more: one pass on the tensor cores.  The unrounded contract
+    // up to 2 activation rows: FMA kernel, each decoded weight feeding every
+    // row; 3 and more: one pass on the tensor cores.  The unrounded contract
     // keeps f32 weights, which the bf16 tensor-core operands cannot carry:
     // FMA passes of up to 4 rows for every M.
     if (p.unrounded) {
@@ -520,9 +528,9 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
         }
     } else {
         switch (p.k) {
-            case 2: e = M <= 4 ? launch_k<2, false>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
-            case 3: e = M <= 4 ? launch_k<3, false>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
-            case 4: e = M <= 4 ? launch_k<4, false>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
+            case 2: e = M < kMmaMinRows ? launch_k<2, false>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
+            case 3: e = M < kMmaMinRows ? launch_k<3, false>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
+            case 4: e = M < kMmaMinRows ? launch_k<4, false>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
             default: return cudaErrorInvalidValue;
         }
     }

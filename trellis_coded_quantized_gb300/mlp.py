@@ -61,12 +61,12 @@ class PackedMLPStack:
 
     def splits_for(self, M: int) -> int:
         """Row splits of the down projection: the constructor's, else one per
-        SM for the FMA scatter (M <= 4), and for the tensor-core scatter the
+        SM for the FMA scatter (M <= 2), and for the tensor-core scatter the
         fewest splits whose row ranges are whole 16-row MMA steps at the
         SM-limited step count (17408 rows on 152 SMs: 136 splits of 128)."""
         if self.splits:
             return self.splits
-        if M <= 4:
+        if M <= 2:
             return self.sm_count
         steps = -(-self.inter // 16)
         per = -(-steps // self.sm_count)
@@ -78,9 +78,9 @@ class PackedMLPStack:
 
     def launches_per_pass(self, M: int) -> int:
         # rmsnorm; gate+up+silu fused (M = 1) or gate, up, silu*up; the
-        # scatter (ceil(M/4) FMA passes up to 4 rows, one tensor-core pass
-        # from 5 rows); the split reduction
-        return len(self.layers) * (1 + (1 if M == 1 else 3) + ((M + 3) // 4 if M <= 4 else 1) + 1)
+        # scatter (one FMA pass up to 2 rows, one tensor-core pass from 3);
+        # the split reduction
+        return len(self.layers) * (1 + (1 if M == 1 else 3) + 1 + 1)
 
     def layer(self, l: int, x, out, keep=None):
         """One layer on x [M, hidden] into out [M, hidden]."""
