@@ -218,7 +218,7 @@ def test_scatter_partials(orc):
         assert np.all(np.abs(part[:, s, :] - ref[:, s, :]) <= 1e-5 * asum + 1e-30), s
 
 
-@pytest.mark.parametrize("M,k", [(16, 3), (5, 2), (32, 4)])
+@pytest.mark.parametrize("M,k", [(16, 3), (5, 2), (32, 4), (3, 3), (4, 4)])
 def test_scatter_tensor_path_full_size(orc, M, k):
     """3 or more activation rows take the tensor-core scatter (one pass)."""
     rows, cols = 17408, 5120
