@@ -211,7 +211,7 @@ class Workload:
         elif w == "scatter":
             self.splits = cf["splits"]
             nt = 1 if self.M <= 8 else 2 if self.M <= 16 else 4
-            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 2 or self.unrounded else
+            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 2 else
                            f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel")
             self.kernel_file = "scatter.cu"
         else:
@@ -239,12 +239,12 @@ class Workload:
             + self.M * nout * 2
         if w == "scatter":   # the split partials are written and read back once
             self.alg_bytes += 2 * self.M * self.splits * cols * 4
-        # the scatter: FMA passes of up to 4 rows (all M when unrounded), or
-        # one tensor-core pass for 3 and more rows; then the split reduction
+        # the scatter: one FMA pass up to 2 rows, one tensor-core pass for 3
+        # and more rows; then the split reduction
         if w != "scatter":
             self.launches_per_step = 1
         else:
-            self.launches_per_step = 1 + ((self.M + 3) // 4 if self.M <= 2 or self.unrounded else 1)
+            self.launches_per_step = 2
 
     def run(self, codes, x=None, out=None):
         tcq = self.tcq

@@ -78,8 +78,10 @@ typedef struct trellis_geometry {
  * contraction in f32 WITHOUT the bf16 rounding.  The kernels apply the scale
  * once per row -- to the row sum on axis 1, to the activation x[m][r] on
  * axis 0 -- which equals the per-weight f32 product up to f32 rounding.
- * Taken by trellis_matvec, trellis_gate_up_matvec and trellis_scatter (and trellis_scatter_noalloc;
- * there all M run on the FMA kernel, 4 activation rows per pass).
+ * Taken by trellis_matvec, trellis_gate_up_matvec and trellis_scatter (and
+ * trellis_scatter_noalloc; from 3 activation rows the scatter's tensor-core
+ * path carries each f32 weight as three bf16 terms, hi + mid + lo, which
+ * keep its 24 significant bits).
  * trellis_prefill and trellis_expand return TRELLIS_ERR_GEOMETRY for it:
  * their tensor-core operands and their output are the rounded bf16 weight.
  */

@@ -268,7 +268,11 @@ __host__ __device__ constexpr int smma_warps(int nt) { return nt == 1 ? 20 : nt 
 // memory once per CTA, so the B operands and scales of a step are
 // conflict-free shared loads (xpitch/2 words = 4 mod 32: lanes (g, c) hit
 // banks 4g + c) instead of global loads that touch 8 lines each.
-template <int K, int NT, bool XS>
+// UNR: the unrounded contract.  The f32 weight w = lut * scale is carried as
+// three bf16 terms, hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi -
+// mid) (each difference exact in f32), contracted by three MMAs: the weight
+// is kept to 24 significant bits, as in the f32 product.
+template <int K, int NT, bool XS, bool UNR>
 __global__ void __launch_bounds__(smma_warps(NT) * 32, 1)
 scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, const float* __restrict__ lut,
@@ -427,13 +431,36 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                     v[q][0] = lut_at(lut_s, win_off_sh<K, kLutRepShift>(wq[q], 15 - 2 * mt) | gofs);
                     v[q][1] = lut_at(lut_s, win_off_sh<K, kLutRepShift>(wq[q], 14 - 2 * mt) | gofs);
                 }
-                uint32_t a[4];
-                a[0] = pack_bf16x2(__fmul_rn(v[0][0], sq[0]), __fmul_rn(v[1][0], sq[1]));
-                a[1] = pack_bf16x2(__fmul_rn(v[0][1], sq[0]), __fmul_rn(v[1][1], sq[1]));
-                a[2] = pack_bf16x2(__fmul_rn(v[2][0], sq[2]), __fmul_rn(v[3][0], sq[3]));
-                a[3] = pack_bf16x2(__fmul_rn(v[2][1], sq[2]), __fmul_rn(v[3][1], sq[3]));
-                #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, cur.bf[nt][0], cur.bf[nt][1]);
+                if constexpr (UNR) {
+                    // fragment register e holds (lo half, hi half) = (w[q0][j], w[q1][j])
+                    float wl[4], wh[4];
+                    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int q0 = 2 * (e >> 1), j = e & 1;
+                        wl[e] = __fmul_rn(v[q0][j], sq[q0]);
+                        wh[e] = __fmul_rn(v[q0 + 1][j], sq[q0 + 1]);
+                    }
+                    #pragma unroll
+                    for (int term = 0; term < 3; ++term) {
+                        uint32_t a[4];
+                        #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            a[e] = pack_bf16x2(wl[e], wh[e]);
+                            wl[e] = __fsub_rn(wl[e], __uint_as_float(a[e] << 16));
+                            wh[e] = __fsub_rn(wh[e], __uint_as_float(a[e] & 0xffff0000u));
+                        }
+                        #pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, cur.bf[nt][0], cur.bf[nt][1]);
+                    }
+                } else {
+                    uint32_t a[4];
+                    a[0] = pack_bf16x2(__fmul_rn(v[0][0], sq[0]), __fmul_rn(v[1][0], sq[1]));
+                    a[1] = pack_bf16x2(__fmul_rn(v[0][1], sq[0]), __fmul_rn(v[1][1], sq[1]));
+                    a[2] = pack_bf16x2(__fmul_rn(v[2][0], sq[2]), __fmul_rn(v[3][0], sq[3]));
+                    a[3] = pack_bf16x2(__fmul_rn(v[2][1], sq[2]), __fmul_rn(v[3][1], sq[3]));
+                    #pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, cur.bf[nt][0], cur.bf[nt][1]);
+                }
             }
             // all lanes are done with this chunk before it is refilled
             __syncwarp();
@@ -461,13 +488,13 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
     }
 }
 
-template <int K, int NT, bool XS>
+template <int K, int NT, bool XS, bool UNR>
 cudaError_t launch_mma_xs(const Packed& p, const uint16_t* x, int M, int splits, int rp, int xpitch, int rp16,
                           size_t smem, float* partial, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT, XS>,
+    cudaError_t e = cudaFuncSetAttribute(scatter_mma_kernel<K, NT, XS, UNR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(scatter_mma_kernel<K, NT, XS>, dim3((unsigned)splits), dim3(smma_warps(NT) * 32), smem, stream,
+    e = launch_pdl(scatter_mma_kernel<K, NT, XS, UNR>, dim3((unsigned)splits), dim3(smma_warps(NT) * 32), smem, stream,
                    x, M, p.codes, p.scales, p.lut, (int)p.rows, (int)p.cols, splits, rp, p.interleave, xpitch, rp16,
                    partial);
     if (e != cudaSuccess) return e;
@@ -479,7 +506,7 @@ cudaError_t launch_mma_xs(const Packed& p, const uint16_t* x, int M, int splits,
 // splits read them from global memory.
 constexpr size_t kXsBudget = 40960;
 
-template <int K, int NT>
+template <int K, int NT, bool UNR>
 cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
                           cudaStream_t stream) {
     const int rp = (int)((p.rows + splits - 1) / splits);
@@ -488,16 +515,16 @@ cudaError_t launch_mma_nt(const Packed& p, const uint16_t* x, int M, int splits,
     const size_t xs_bytes = (size_t)NT * 8 * xpitch * 2 + (size_t)rp16 * 4;
     const size_t base = kLutRepBytes + (size_t)smma_warps(NT) * 2 * 16 * (K == 3 ? 20 : 4 * K + 4) * sizeof(uint32_t);
     if (xs_bytes <= kXsBudget)
-        return launch_mma_xs<K, NT, true>(p, x, M, splits, rp, xpitch, rp16, base + xs_bytes, partial, stream);
-    return launch_mma_xs<K, NT, false>(p, x, M, splits, rp, 0, rp16, base, partial, stream);
+        return launch_mma_xs<K, NT, true, UNR>(p, x, M, splits, rp, xpitch, rp16, base + xs_bytes, partial, stream);
+    return launch_mma_xs<K, NT, false, UNR>(p, x, M, splits, rp, 0, rp16, base, partial, stream);
 }
 
-template <int K>
+template <int K, bool UNR>
 cudaError_t launch_mma(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
                        cudaStream_t stream) {
-    if (M <= 8) return launch_mma_nt<K, 1>(p, x, M, splits, partial, stream);
-    if (M <= 16) return launch_mma_nt<K, 2>(p, x, M, splits, partial, stream);
-    return launch_mma_nt<K, 4>(p, x, M, splits, partial, stream);
+    if (M <= 8) return launch_mma_nt<K, 1, UNR>(p, x, M, splits, partial, stream);
+    if (M <= 16) return launch_mma_nt<K, 2, UNR>(p, x, M, splits, partial, stream);
+    return launch_mma_nt<K, 4, UNR>(p, x, M, splits, partial, stream);
 }
 
 }  // namespace
@@ -516,23 +543,17 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     (void)sm_count;
     cudaError_t e;
     // up to 2 activation rows: FMA kernel, each decoded weight feeding every
-    // row; 3 and more: one pass on the tensor cores.  The unrounded contract
-    // keeps f32 weights, which the bf16 tensor-core operands cannot carry:
-    // FMA passes of up to 4 rows for every M.
-    if (p.unrounded) {
-        switch (p.k) {
-            case 2: e = launch_k<2, true>(p, x, M, splits, partial, stream); break;
-            case 3: e = launch_k<3, true>(p, x, M, splits, partial, stream); break;
-            case 4: e = launch_k<4, true>(p, x, M, splits, partial, stream); break;
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (p.k) {
-            case 2: e = M < kMmaMinRows ? launch_k<2, false>(p, x, M, splits, partial, stream) : launch_mma<2>(p, x, M, splits, partial, stream); break;
-            case 3: e = M < kMmaMinRows ? launch_k<3, false>(p, x, M, splits, partial, stream) : launch_mma<3>(p, x, M, splits, partial, stream); break;
-            case 4: e = M < kMmaMinRows ? launch_k<4, false>(p, x, M, splits, partial, stream) : launch_mma<4>(p, x, M, splits, partial, stream); break;
-            default: return cudaErrorInvalidValue;
-        }
+    // row; 3 and more: one pass on the tensor cores (under the unrounded
+    // contract with each f32 weight as three bf16 terms)
+    const bool fma = M < kMmaMinRows;
+    switch (p.k * 2 + (p.unrounded ? 1 : 0)) {
+        case 4: e = fma ? launch_k<2, false>(p, x, M, splits, partial, stream) : launch_mma<2, false>(p, x, M, splits, partial, stream); break;
+        case 5: e = fma ? launch_k<2, true>(p, x, M, splits, partial, stream) : launch_mma<2, true>(p, x, M, splits, partial, stream); break;
+        case 6: e = fma ? launch_k<3, false>(p, x, M, splits, partial, stream) : launch_mma<3, false>(p, x, M, splits, partial, stream); break;
+        case 7: e = fma ? launch_k<3, true>(p, x, M, splits, partial, stream) : launch_mma<3, true>(p, x, M, splits, partial, stream); break;
+        case 8: e = fma ? launch_k<4, false>(p, x, M, splits, partial, stream) : launch_mma<4, false>(p, x, M, splits, partial, stream); break;
+        case 9: e = fma ? launch_k<4, true>(p, x, M, splits, partial, stream) : launch_mma<4, true>(p, x, M, splits, partial, stream); break;
+        default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     const int C = (int)p.cols;
