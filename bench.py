@@ -10,7 +10,10 @@ Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize(); every launch is also bracketed by CUDA events on the
 stream it runs on (the kernel's average duration feeds the roofline).  Steps
 rotate over weight sets totalling > 4x L2, so every step streams its codes
-from HBM.  nvidia-smi samples clocks during the timed region.
+from HBM.  NVML is polled for the SM clock and throttle reasons during the
+timed region.  The shared-memory gather rate is measured first in the same
+run: every decoded weight costs one codebook gather, so weights / rate is a
+floor on each kernel's time, reported beside the HBM fraction.
 
 `--impl reference` times the CPU oracle (the only reference there is) on a
 bounded sample of the same workload.  Under torchrun each rank runs its own
@@ -87,59 +90,116 @@ def profiled_traffic(kernel_file: str, kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """SM clock and throttle-reason samples while running.
+
+    NVML (libnvidia-ml, loaded with ctypes) is polled back to back from a
+    thread, about every 0.2 ms, so that even a timed region of well under a
+    millisecond gets samples; each sample carries its host time, and
+    `summary(t0, t1)` keeps the samples taken between t0 and t1.  Without
+    NVML, nvidia-smi is sampled every 200 ms instead."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.samples = []        # (host time, sm MHz, sm max MHz, reason bits or None, reason names)
+        self.source = None
+        self._stop = threading.Event()
+        self.thread = None
+
+    def _nvml(self):
+        import ctypes
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            return None
+        return lib, h
 
     def __enter__(self):
+        nv = None
+        try:
+            nv = self._nvml()
+        except Exception:
+            nv = None
+        if nv is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, args=nv, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
         return self
 
-    def _read(self):
+    def _poll_nvml(self, lib, h):
+        import ctypes
+        clk, cmax, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(cmax))
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:       # NVML_CLOCK_SM
+                bits = None
+                if get_reasons is not None and get_reasons(h, ctypes.byref(rs)) == 0:
+                    bits = int(rs.value)
+                names = [n for b, n in self.REASONS.items() if bits is not None and bits & b]
+                self.samples.append((time.perf_counter(), float(clk.value), float(cmax.value), bits, names))
+            time.sleep(0.0002)
+
+    def _read_smi(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, smax = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            names = [n for n, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"],
+                                       f[5:9]) if v.lower().startswith("active")]
+            self.samples.append((time.perf_counter(), sm, smax, None, names))
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, the largest max clock and every active throttle
+        reason of the samples taken between host times t0 and t1 (all
+        samples when not given)."""
+        sel = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        reasons = sorted({n for x in sel for n in x[4]})
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+                "reasons": reasons, "samples": len(sel), "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -234,11 +294,15 @@ class Workload:
         if w == "scatter":
             self.ws = torch.empty(tcq.trellis_scatter_workspace_bytes(self.g, self.M, self.splits) // 4,
                                   dtype=torch.float32, device=device)
-        # algorithmic bytes of the dominant launch: codes, scales, codebook, x, out
+        # algorithmic bytes of the step: the method's inputs and output --
+        # codes, scales, codebook, x, out.  The scatter's fp32 split partials
+        # are the implementation's buffer (written and read back once, mostly
+        # in L2) and are reported apart as partial_bytes.
         self.alg_bytes = self.packed + rows * 2 + 4096 * 4 + self.M * (cols if self.axis == 1 else rows) * 2 \
             + self.M * nout * 2
-        if w == "scatter":   # the split partials are written and read back once
-            self.alg_bytes += 2 * self.M * self.splits * cols * 4
+        self.partial_bytes = 2 * self.M * self.splits * cols * 4 if w == "scatter" else 0
+        # decoded weights per step: one codebook gather each
+        self.weights = rows * cols
         # the scatter: one FMA pass up to 2 rows, one tensor-core pass for 3
         # and more rows; then the split reduction
         if w != "scatter":
@@ -308,8 +372,42 @@ def time_launches(torch, fn, steps, warmup, stream, barrier, per_launch=True):
     return total_ms, per
 
 
-def secondary(torch, tcq, device, stream, peaks, l2):
-    """Median launch times of the other configurations (context figures)."""
+def gather_rates(torch, tcq, device, stream, clk):
+    """Shared-memory gather rate, the ceiling of the decode (one random
+    4-byte codebook read per weight), with 1, 4 and 8 interleaved table
+    copies: gathers per second on the whole GPU, and per SM and clock at the
+    SM clock sampled while the probe ran."""
+    lut = torch.randn(4096, device=device)
+    sm = torch.cuda.get_device_properties(device).multi_processor_count
+    iters = 2000
+    out = {}
+    for rep in (1, 4, 8):
+        h0 = time.perf_counter()
+        _, per = time_launches(torch, lambda i: tcq.trellis_gather_probe(lut, sm, iters, rep), 5, 2,
+                               stream, lambda: None)
+        h1 = time.perf_counter()
+        t = statistics.median(per) * 1e-3
+        gathers = sm * 1024 * iters * 8
+        mhz = clk.summary(h0, h1)["sm_mhz"] or 2070.0
+        out[f"smem_gather_x{rep}"] = {"gathers_per_s": gathers / t, "sm_mhz": mhz,
+                                      "per_sm_per_clock": round(gathers / t / sm / (mhz * 1e6), 3)}
+    return out, sm
+
+
+def gather_floor_s(weights: float, rates: dict, sm: int, sm_mhz) -> float:
+    """Shortest time the decode of `weights` weights can take: one gather each
+    at the measured 8-copy rate (per SM and clock) on all SMs at the sampled
+    median SM clock of the run."""
+    r = rates["smem_gather_x8"]
+    mhz = sm_mhz or r["sm_mhz"]
+    return weights / (r["per_sm_per_clock"] * sm * mhz * 1e6)
+
+
+def secondary(torch, tcq, device, stream, peaks, l2, rates, sm, sm_mhz):
+    """Launch times of the other configurations (context figures): `us` is
+    the median of launches each bracketed by events, `us_back_to_back` the
+    average over 100 launches in a row.  Each line carries its fraction of
+    HBM (algorithmic bytes) and of the gather floor."""
     out = {}
     hbm = peaks["hbm_gbs"]
     tc_peak = peaks["bf16_tflops"]
@@ -319,7 +417,8 @@ def secondary(torch, tcq, device, stream, peaks, l2):
     for w, M, k, S, unr in ([("prefill", M, k, 0, False) for k in (2, 3, 4) for M in (5, 8, 16, 32)] +
                             [("scatter", 1, 3, 128, False), ("scatter", 4, 3, 128, False),
                              ("scatter", 1, 3, 152, False), ("scatter", 4, 3, 152, False),
-                             ("scatter", 16, 3, 128, False), ("tiny-matvec", 1, 2, 0, False),
+                             ("scatter", 16, 3, 128, False), ("scatter", 16, 3, 8, False),
+                             ("scatter", 32, 3, 8, False), ("tiny-matvec", 1, 2, 0, False),
                              ("decode-matvec", 1, 4, 0, True), ("scatter", 1, 3, 128, True),
                              ("scatter", 4, 3, 128, True), ("scatter", 16, 3, 128, True)]):
         a = A()
@@ -328,13 +427,20 @@ def secondary(torch, tcq, device, stream, peaks, l2):
         _, per = time_launches(torch, wl.step, 30, 3, stream, lambda: None)
         t = statistics.median(per) * 1e-3
         tb, _ = time_launches(torch, wl.step, 100, 3, stream, lambda: None, per_launch=False)
+        tb = tb * 1e-3 / 100
         key = f"{w}_M{M}_k{k}" + (f"_s{S}" if w == "scatter" else "") + ("_unrounded" if unr else "")
-        rec = {"us": round(t * 1e6, 2), "us_back_to_back": round(tb * 10, 2), "packed_gbs": round(wl.packed / t / 1e9, 1),
-               "tokens_per_s": round(M / t, 1), "frac_of_hbm_alg": round(wl.alg_bytes / t / 1e9 / hbm, 4)}
+        floor = gather_floor_s(wl.weights, rates, sm, sm_mhz)
+        rec = {"us": round(t * 1e6, 2), "us_back_to_back": round(tb * 1e6, 2),
+               "packed_gbs": round(wl.packed / tb / 1e9, 1), "tokens_per_s": round(M / tb, 1),
+               "frac_of_hbm_alg": round(wl.alg_bytes / tb / 1e9 / hbm, 4),
+               "gather_floor_us": round(floor * 1e6, 2), "frac_of_gather_floor": round(floor / tb, 4),
+               "frac_of_gather_floor_isolated": round(floor / t, 4)}
+        if w == "scatter":
+            rec["partial_bytes"] = wl.partial_bytes
         if w == "prefill":
             roof = min(hbm * 1e9 * wl.flops / wl.packed, tc_peak * 1e12)
-            rec["tflops"] = round(wl.flops / t / 1e12, 2)
-            rec["frac_of_roofline"] = round(wl.flops / t / roof, 4)
+            rec["tflops"] = round(wl.flops / tb / 1e12, 2)
+            rec["frac_of_roofline"] = round(wl.flops / tb / roof, 4)
         out[key] = rec
         del wl
         torch.cuda.empty_cache()
@@ -342,45 +448,39 @@ def secondary(torch, tcq, device, stream, peaks, l2):
     from trellis_coded_quantized_gb300.mlp import PackedMLPStack
     stack = PackedMLPStack(layers=40, k=3, device=device, m_max=16)
     from trellis_coded_quantized_gb300 import synth
+    weights = len(stack.layers) * 3 * stack.inter * stack.hidden
+    floor = gather_floor_s(weights, rates, sm, sm_mhz)
     for M in (1, 16):
         x0 = torch.from_numpy(synth.activations(0, M, 5120).view(np.int16)).to(device).view(torch.bfloat16)
-        _, per = time_launches(torch, lambda i: stack.forward(x0), 5, 2, stream, lambda: None)
+        _, per = time_launches(torch, lambda i: stack.forward(x0, check=False), 5, 2, stream, lambda: None)
         t = statistics.median(per) * 1e-3
         rec = {"ms_per_pass": round(t * 1e3, 3), "tokens_per_s": round(M / t, 1),
                "packed_gbs": round(stack.packed_bytes / t / 1e9, 1),
-               "tflops": round(2.0 * M * stack.packed_bytes * 8 / 3 / t / 1e12, 2),
-               "launches_per_pass": stack.launches_per_pass(M)}
+               "tflops": round(2.0 * M * weights / t / 1e12, 2),
+               "launches_per_pass": stack.launches_per_pass(M),
+               "gather_floor_ms": round(floor * 1e3, 3), "frac_of_gather_floor": round(floor / t, 4)}
         # the same pass captured once in a CUDA graph and replayed
         try:
             graph = torch.cuda.CUDAGraph()
             side = torch.cuda.Stream()
             side.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(side):
-                stack.forward(x0)
+                stack.forward(x0, check=False)
             torch.cuda.current_stream().wait_stream(side)
             with torch.cuda.graph(graph):
-                stack.forward(x0)
+                stack.forward(x0, check=False)
             _, per = time_launches(torch, lambda i: graph.replay(), 5, 2, stream, lambda: None)
             tg = statistics.median(per) * 1e-3
             rec["graph_ms_per_pass"] = round(tg * 1e3, 3)
             rec["graph_tokens_per_s"] = round(M / tg, 1)
+            rec["graph_frac_of_gather_floor"] = round(floor / tg, 4)
             del graph
         except Exception as e:          # report, do not fail the bench line
             rec["graph_error"] = str(e)[:200]
         out[f"mlp40_M{M}_k3"] = rec
     del stack
     torch.cuda.empty_cache()
-    # shared-memory gather rate (the decode's second roofline), with 1, 4 and 8 table copies
-    lut = torch.randn(4096, device=device)
-    sm = torch.cuda.get_device_properties(device).multi_processor_count
-    iters = 2000
-    for rep in (1, 4, 8):
-        _, per = time_launches(torch, lambda i: tcq.trellis_gather_probe(lut, sm, iters, rep), 5, 2,
-                               stream, lambda: None)
-        t = statistics.median(per) * 1e-3
-        gathers = sm * 1024 * iters * 8
-        out[f"smem_gather_x{rep}"] = {"gathers_per_s": gathers / t,
-                                      "per_sm_per_clock_at_2070MHz": round(gathers / t / sm / 2.07e9, 3)}
+    out.update(rates)
     return out
 
 
@@ -401,10 +501,19 @@ def run_ours(args):
 
     wl = Workload(args, torch, tcq, device, l2)
     with ClockSampler(local_rank) as clk:
+        # the gather ceiling of this run, measured first on the same GPU
+        rates, sm = gather_rates(torch, tcq, device, stream, clk)
+        h0 = time.perf_counter()
         total_ms, _ = time_launches(torch, wl.step, args.steps, args.warmup, stream, barrier, per_launch=False)
-    total_ms = max_over_ranks(torch, dist, total_ms, device)
-    # the same launches one at a time, each between two events (context only)
-    _, per = time_launches(torch, wl.step, min(args.steps, 2000), 3, stream, lambda: None)
+        h1 = time.perf_counter()
+        total_ms = max_over_ranks(torch, dist, total_ms, device)
+        # the same launches one at a time, each between two events (context only)
+        h2 = time.perf_counter()
+        _, per = time_launches(torch, wl.step, min(args.steps, 2000), 3, stream, lambda: None)
+        h3 = time.perf_counter()
+    clocks = clk.summary(h0, h1)
+    clocks_all = clk.summary(h0, h3)
+    sm_mhz = clocks["sm_mhz"] or clocks_all["sm_mhz"]
     ms = total_ms / args.steps
     sec = total_ms * 1e-3
     if wl.name == "prefill":
@@ -418,12 +527,19 @@ def run_ours(args):
     # start with the previous one's tail
     kern_s = ms * 1e-3
     achieved = wl.alg_bytes / kern_s / 1e9
+    iso_s = statistics.median(per) * 1e-3
+    floor = gather_floor_s(wl.weights, rates, sm, sm_mhz)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": profiled_traffic(wl.kernel_file, wl.kernel), "kernel": wl.kernel,
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)", "kernel_us": round(kern_s * 1e6, 3),
-                "kernel_us_isolated": round(statistics.median(per) * 1e3, 3),
-                "algorithmic_bytes": wl.alg_bytes}
+                "kernel_us_isolated": round(iso_s * 1e6, 3),
+                "algorithmic_bytes": wl.alg_bytes, "partial_bytes": wl.partial_bytes,
+                "gather_floor_us": round(floor * 1e6, 3), "frac_of_gather_floor": round(floor / kern_s, 4),
+                "frac_of_gather_floor_isolated": round(floor / iso_s, 4),
+                "gather_rate_per_sm_per_clock": rates["smem_gather_x8"]["per_sm_per_clock"],
+                "gather_floor_basis": f"{wl.weights} weights x 1 shared-memory gather at the measured 8-copy rate "
+                                      f"on {sm} SMs at {sm_mhz} MHz"}
 
     # end to end: pinned host inputs -> device, the C-ABI call, result -> host
     h = {"codes": torch.from_numpy(wl.p["codes"].view(np.int32)).pin_memory(),
@@ -482,7 +598,7 @@ def run_ours(args):
     if rank == 0 and not args.no_extras:
         del wl.sets
         torch.cuda.empty_cache()
-        extras = secondary(torch, tcq, device, stream, peaks, l2)
+        extras = secondary(torch, tcq, device, stream, peaks, l2, rates, sm, sm_mhz)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -501,7 +617,8 @@ def run_ours(args):
                              f"({wl.nsets * wl.packed / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * wl.launches_per_step, "clocks": clk.summary(),
+            "gpu_launches": args.steps * wl.launches_per_step, "clocks": clocks,
+            "clocks_whole_measurement": clocks_all,
             "device_status": status, "secondary": extras,
         }
         print(json.dumps(line))
@@ -513,46 +630,85 @@ def run_ours(args):
 # the oracle as the CPU baseline / reference arm
 # ---------------------------------------------------------------------------
 
-def oracle_pass(orc, wl, rows):
-    """The oracle on the first `rows` rows of the workload's packed matrix:
-    expand them to bf16 weights, then the double contraction (axis 1: those
-    output rows; axis 0: the sum over those input rows)."""
+def oracle_parts(orc, wl, rows):
+    """The oracle on the first `rows` rows of the workload's packed matrix,
+    its two steps timed apart: (seconds to expand them to weights, seconds of
+    the double contraction -- axis 1: those output rows; axis 0: the sum over
+    those input rows)."""
     p = wl.p
     codes = p["codes"][:rows]
+    unr = getattr(wl, "unrounded", False)
     t0 = time.perf_counter()
-    if getattr(wl, "unrounded", False):        # the unrounded contract: f32 weights
+    if unr:                                     # the unrounded contract: f32 weights
         W = orc.expand_f32(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
-        if wl.axis == 1:
-            orc.matmul_axis1_f32w(p["x"], W)
-        else:
-            orc.matmul_axis0_f32w(p["x"][:, :rows], W)
-        return time.perf_counter() - t0
-    W, _ = orc.expand(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
-    if wl.axis == 1:
-        orc.matmul_axis1(p["x"], W)
     else:
-        orc.matmul_axis0(p["x"][:, :rows], W)
-    return time.perf_counter() - t0
+        W, _ = orc.expand(codes, rows, wl.cols, wl.k, p["scales"][:rows], p["lut"])
+    t1 = time.perf_counter()
+    if wl.axis == 1:
+        (orc.matmul_axis1_f32w if unr else orc.matmul_axis1)(p["x"], W)
+    else:
+        (orc.matmul_axis0_f32w if unr else orc.matmul_axis0)(p["x"][:, :rows], W)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def oracle_pass(orc, wl, rows):
+    """Seconds of one oracle pass (expansion + contraction) over `rows` rows."""
+    a, b = oracle_parts(orc, wl, rows)
+    return a + b
+
+
+def _timed_parts(orc, wl, seconds):
+    """Rows, expansion seconds and contraction seconds of repeated oracle
+    passes filling about `seconds` of wall-clock time."""
+    t = oracle_pass(orc, wl, min(wl.rows, 16))
+    rows = int(min(wl.rows, max(8, 16 * (seconds / 4) / max(t, 1e-6))))   # a pass of about a quarter of the time
+    done_rows, te, tm, t0 = 0, 0.0, 0.0, time.perf_counter()
+    while True:
+        a, b = oracle_parts(orc, wl, rows)
+        done_rows, te, tm = done_rows + rows, te + a, tm + b
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return done_rows, te, tm
 
 
 def cpu_baseline(wl, seconds: float = 10.0):
+    """The oracle as it stands on this host's cores: expansion (packed GB/s)
+    and double contraction (GFLOP/s) timed apart, each on 1 thread and on
+    all cores, on a bounded sample of the workload's rows; `value` is the
+    whole pass on all cores in the metric's unit."""
     import oracle
     orc = oracle.default()
-    t = oracle_pass(orc, wl, min(wl.rows, 256))
-    rows = int(min(wl.rows, max(16, 256 * 1.0 / max(t, 1e-6))))   # about a second per pass
-    done_rows, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        oracle_pass(orc, wl, rows)
-        done_rows += rows
-    el = time.perf_counter() - t0
-    frac = done_rows / wl.rows
+    cores = orc.max_threads()
+    parts = {}
+    try:
+        for label, threads in (("1_thread", 1), ("all_cores", cores)):
+            orc.set_threads(threads)
+            n, te, tm = _timed_parts(orc, wl, seconds / 2)
+            frac = n / wl.rows
+            parts[label] = {"threads": threads, "rows": n,
+                            "expand_gbs": round(frac * wl.packed / te / 1e9, 6),
+                            "expand_weights_per_s": round(n * wl.cols / te, 1),
+                            "matmul_gflops": round(frac * wl.flops / tm / 1e9, 6),
+                            "expand_s": round(te, 3), "matmul_s": round(tm, 3)}
+    finally:
+        orc.set_threads(cores)
+    a = parts["all_cores"]
+    frac = a["rows"] / wl.rows
+    el = a["expand_s"] + a["matmul_s"]
     if wl.name == "prefill":
         value, unit = frac * wl.flops / el / 1e12, "TFLOP/s"
     else:
         value, unit = frac * wl.packed / el / 1e9, "GB/s"
-    return {"value": round(value, 6), "unit": unit, "cores": orc.max_threads(), "kind": "oracle",
-            "sample": f"{done_rows} of the {wl.rows} matrix rows ({rows} per pass: expand to bf16 weights "
-                      f"+ double contraction), {el:.1f} s"}
+    return {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"expansion to weights + double contraction of the first rows of the {wl.rows}-row matrix: "
+                      f"{parts['1_thread']['rows']} rows on 1 thread, {a['rows']} rows on {cores} threads, "
+                      f"about {seconds / 2:.0f} s each",
+            "expand": {"unit": "GB/s packed", "1_thread": parts["1_thread"]["expand_gbs"],
+                       "all_cores": a["expand_gbs"]},
+            "matmul": {"unit": "GFLOP/s (double)", "1_thread": parts["1_thread"]["matmul_gflops"],
+                       "all_cores": a["matmul_gflops"]},
+            "parts": parts}
 
 
 class _HostWorkload:

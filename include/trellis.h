@@ -19,7 +19,9 @@
  *     (cudaSetDevice before the call).  bf16 arrays are IEEE bfloat16 bit
  *     patterns (uint16), row-major.  The caller owns and allocates every
  *     buffer, inputs, outputs and workspace; the library allocates no memory
- *     and keeps no pointer after the call returns.
+ *     and keeps no pointer after the call returns.  One exception:
+ *     trellis_scatter_noalloc keeps its split partials in a fixed 16 MiB
+ *     device array that the library itself declares (see there).
  *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  Work is
  *     only enqueued: the call never synchronises.  Results are valid once
  *     the stream has reached the work.
@@ -29,7 +31,8 @@
  *     gives up records a code readable with trellis_device_status().
  *   - codes are rows*(cols/256)*wpb uint32 words in the geometry's block
  *     layout (see trellis_geometry).  scales are
- *     bf16 [rows].  lut is f32 [4096].  codes and x must be 16-byte aligned.
+ *     bf16 [rows].  lut is f32 [4096].  codes, x and lut must be 16-byte
+ *     aligned; so must out and workspace of the scatter.
  */
 #ifndef TRELLIS_H
 #define TRELLIS_H
@@ -149,11 +152,18 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
  * [s*rp, min(rows, (s+1)*rp)) and may be empty.  fp32 partial sums go to
  * workspace [M, splits, cols] and a second kernel sums them over the split
  * axis in split order and rounds to bf16.
- *   x          bf16 [M, rows]
- *   splits     1..1024, or 0 for the default of 128
+ *   x          bf16 [M, rows], 16-byte aligned
+ *   splits     1..1024, or 0 for the default: 128 when M <= 4 (scatter.ts,
+ *              SCATTER_SPLITS), else the split count of the split-K
+ *              launcher (splitk-prefill.ts): with tilesM = ceil(M/32),
+ *              tilesN = ceil(cols/32), tilesK = floor(rows/16) and
+ *              ratio = max(1, floor(tilesK / (tilesM*tilesN))), the power of
+ *              two at or above ratio, clamped to [2, 32] (8 at 17408 x 5120)
  *   workspace  f32, at least trellis_scatter_workspace_bytes(g, M, splits) bytes,
- *              16-byte aligned; contents on entry do not matter
- *   out        bf16 [M, cols]     out[m][c] = bf16( sum_r x[m][r] w[r][c] )
+ *              16-byte aligned; contents on entry do not matter.  On return
+ *              it holds the partials P[m][s][c] (empty ranges hold zeros).
+ *   out        bf16 [M, cols], 16-byte aligned
+ *              out[m][c] = bf16( sum_r x[m][r] w[r][c] )
  * Requires g->axis == 0.
  */
 trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
@@ -171,11 +181,17 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
  * the fp32 split partials go to a 16 MiB array of device memory that the
  * library declares itself (reserved on every GPU that loads the library
  * until the process exits).
- *   - M * splits * cols must be at most 4,194,304 (splits 0 means 128),
- *     else TRELLIS_ERR_WORKSPACE and nothing is enqueued;
+ *   - x and out must be 16-byte aligned, as for trellis_scatter;
+ *   - M * splits * cols must be at most 4,194,304 (splits 0 is resolved as
+ *     for trellis_scatter), else TRELLIS_ERR_WORKSPACE and nothing is
+ *     enqueued;
  *   - allocates nothing; the first call on a device looks up the array's
- *     device address (cudaGetSymbolAddress), so make that first call before
- *     any stream capture;
+ *     device address (cudaGetSymbolAddress).  With CUDA's lazy module
+ *     loading the driver reserves the array when the library's scatter code
+ *     is first used on that device -- the first trellis_scatter or
+ *     trellis_scatter_noalloc call -- and that first use may synchronise.
+ *     So make one such call on each device before any stream capture or any
+ *     region where device allocation is not allowed;
  *   - all calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
  */
@@ -184,7 +200,12 @@ trellis_status trellis_scatter_noalloc(const void* x, int32_t M, const uint32_t*
                                        const trellis_geometry* g, int32_t splits,
                                        void* out, void* stream);
 
-/* M * splits * cols * 4 bytes (splits 0 means 128); 0 for invalid arguments. */
+/*
+ * Bytes of workspace trellis_scatter needs: the fp32 partials
+ * [M, splits, cols] of the scatter launch (scatter.ts, the [M, SPLITS, C]
+ * float partial output), M * splits * cols * 4, with splits 0 resolved as
+ * trellis_scatter does.  0 for invalid arguments.
+ */
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits);
 
 /*
@@ -231,7 +252,12 @@ trellis_status trellis_gather_probe(const float* lut, int32_t blocks, int32_t it
  */
 trellis_status trellis_device_status(int32_t* status);
 
-/* Static English text for a status; never NULL. */
+/*
+ * Static English text for a status; never NULL.  The pages report an
+ * unsupported geometry by throwing with a message (tiled-prefill.ts and
+ * splitk-prefill.ts, launchers); this library returns the status and this
+ * text describes it.
+ */
 const char* trellis_strerror(trellis_status status);
 
 #ifdef __cplusplus

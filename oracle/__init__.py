@@ -107,6 +107,8 @@ class Oracle:
         lib.tcq_oracle_matmul_axis0_f32w.argtypes = [P, I64, P, I64, I64, I64, P, P, P, P]
         lib.tcq_oracle_rmsnorm.argtypes = [P, I64, I64, ctypes.c_double, P]
         lib.tcq_oracle_silu_mul.argtypes = [P, P, I64, P]
+        lib.tcq_oracle_scatter_default_splits.argtypes = [I64, I64, I64]
+        lib.tcq_oracle_scatter_default_splits.restype = I64
         self.lib = lib
         self.path = path
 
@@ -259,6 +261,11 @@ class Oracle:
         out = np.empty_like(g)
         self.lib.tcq_oracle_silu_mul(_ptr(g), _ptr(u), g.size, _ptr(out))
         return out
+
+    # -- split count ----------------------------------------------------------
+    def scatter_default_splits(self, rows: int, cols: int, M: int) -> int:
+        """Row splits of the axis-0 scatter when the caller gives none."""
+        return int(self.lib.tcq_oracle_scatter_default_splits(rows, cols, M))
 
     # -- the tolerance of the contraction ------------------------------------
     def within_tolerance(self, got_bf16, y, a, rel: float = 4e-3):

@@ -429,3 +429,30 @@ void tcq_oracle_matmul_axis0_f32w(const uint16_t* x, int64_t M, const float* w,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* default split count of the axis-0 scatter                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The number of row splits the scatter uses when the caller leaves it open.
+ * Up to 4 activation rows: the scatter launch's fixed SCATTER_SPLITS = 128
+ * (@mlx-bun/inference 1.0.0, kernels/trellis/scatter.ts).  From 5 rows: the
+ * split-K launcher's rule (kernels/trellis/splitk-prefill.ts, the launcher):
+ * tilesM = ceil(M/32), tilesN = ceil(cols/32), tilesK = floor(rows/16),
+ * ratio = max(1, floor(tilesK / (tilesM * tilesN))),
+ * splits = min(32, max(2, 2^ceil(log2(ratio)))).
+ * Written with the pages' floating-point formulation.
+ */
+int64_t tcq_oracle_scatter_default_splits(int64_t rows, int64_t cols, int64_t M) {
+    if (M <= 4) return 128;
+    double tiles_m = ceil((double)M / 32.0);
+    double tiles_n = ceil((double)cols / 32.0);
+    double tiles_k = floor((double)rows / 16.0);
+    double ratio = floor(tiles_k / (tiles_m * tiles_n));
+    if (ratio < 1.0) ratio = 1.0;
+    double s = pow(2.0, ceil(log2(ratio)));
+    if (s < 2.0) s = 2.0;
+    if (s > 32.0) s = 32.0;
+    return (int64_t)s;
+}

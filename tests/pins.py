@@ -275,12 +275,13 @@ def check_expand_layout(o: _o.Oracle, seed: int = 13):
                 blk = codes[r * nb * wpb + b * wpb:][:wpb]
                 for t in (0, 1, 77, 255):
                     assert win[r, b * BT + t] == window_by_string(blk, k, t)
-        # interleave 2 holds the same blocks at other addresses
-        inter = np.empty(_o.code_words(rows, cols, k, 2), np.uint32)
-        for r in range(rows):
-            for b in range(nb):
-                base = (b // 2) * rows * 2 * wpb + r * 2 * wpb + (b % 2) * wpb
-                inter[base:base + wpb] = codes[r * nb * wpb + b * wpb:][:wpb]
+        # interleave 2 holds the same blocks at other addresses: built here by
+        # array reshaping alone, without the address formula -- view the
+        # row-major codes as [row][block pair][pair member, words], move the
+        # block-pair axis outermost, and flatten
+        inter = np.ascontiguousarray(
+            codes.reshape(rows, nb // 2, 2 * wpb).transpose(1, 0, 2)).reshape(-1)
+        assert inter.size == _o.code_words(rows, cols, k, 2)
         _, win2 = o.expand(inter, rows, cols, k, sc, lut, interleave=2)
         assert np.array_equal(win, win2)
 
@@ -493,6 +494,24 @@ def check_unrounded_contract(o: _o.Oracle, seed: int = 43):
         assert np.allclose(part[:, s, :], want, rtol=1e-12, atol=1e-12), s
 
 
+def read_default_splits():
+    """(rows, cols, M, splits) rows of tests/golden/default_splits.txt."""
+    out = []
+    with open(os.path.join(GOLDEN, "default_splits.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                out.append(tuple(int(v) for v in line))
+    return out
+
+
+def check_default_splits(o: _o.Oracle):
+    """The default split count of the scatter against values worked by hand
+    from the split-K launcher's rule (and 128 up to 4 activation rows)."""
+    for rows, cols, M, want in read_default_splits():
+        assert o.scatter_default_splits(rows, cols, M) == want, (rows, cols, M)
+
+
 ALL_CHECKS = [
     check_golden_windows, check_windows_random, check_single_bit_probes,
     check_wrap_and_rotation, check_special_patterns, check_bf16_rounding,
@@ -500,4 +519,5 @@ ALL_CHECKS = [
     check_contraction_vs_numpy, check_unit_vectors_and_bilinear,
     check_reductions, check_lut_readback, check_brute_force_tiny,
     check_sampled_matches_full, check_glue, check_unrounded_contract,
+    check_default_splits,
 ]

@@ -113,6 +113,18 @@ def test_workspace_size(lib):
     assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, _p(A), need - 4, _p(A), None) == WORKSPACE
 
 
+def test_default_split_count(lib):
+    """splits = 0: 128 up to 4 activation rows, else the split-K launcher's
+    rule (the hand-worked values of tests/golden/default_splits.txt)."""
+    import pins
+    for rows, cols, M, want in pins.read_default_splits():
+        g0 = geometry(0, rows, cols, 3)
+        assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), M, 0) == M * want * cols * 4, (rows, cols, M)
+    g0 = geometry(0, 17408, 5120, 3)
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 0) == 4 * 128 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 8, 0) == 8 * 8 * 5120 * 4
+
+
 def test_glue_validation(lib):
     assert lib.trellis_rmsnorm(None, 1, 16, ctypes.c_float(1e-6), _p(A), None) == NULL
     assert lib.trellis_rmsnorm(_p(A), 1, 70000, ctypes.c_float(1e-6), _p(A), None) == SHAPE

@@ -36,6 +36,8 @@ MUTANTS = {
     "silu_sign": ("gv / (1.0 + exp(-gv)) * uv", "gv / (1.0 + exp(gv)) * uv"),
     "unrounded_weight_rounded": ("w_out[r * cols + c] = (float)((double)lut[win] * (double)s);",
                                  "w_out[r * cols + c] = tcq_oracle_bf16_to_float(tcq_oracle_bf16_from_double((double)lut[win] * (double)s));"),
+    "default_splits_floor_log2": ("double s = pow(2.0, ceil(log2(ratio)));", "double s = pow(2.0, floor(log2(ratio)));"),
+    "default_splits_no_row_tiles": ("double tiles_k = floor((double)rows / 16.0);", "double tiles_k = floor((double)rows / 32.0);"),
     "unrounded_axis0_transposed": ("(double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[r * cols + c];",
                                    "(double)tcq_oracle_bf16_to_float(x[m * rows + r]) * (double)w[c * rows + r];"),
 }

@@ -174,6 +174,67 @@ def test_rounded_paths_agree_with_their_own_oracle(orc):
     assert np.mean(out_unr != out_rnd) >= DISAGREE
 
 
+_FULL = {}
+
+
+def _full_size(orc, axis, k, M, seed):
+    """A 17408 x 5120 problem of the given axis and its rounded expansion
+    (cached per axis and k: the expansion takes a while)."""
+    rows, cols = 17408, 5120
+    key = (axis, k)
+    if key not in _FULL:
+        p0 = synth.problem(axis, 1, rows, cols, k, seed=seed)
+        wb, _ = orc.expand(p0["codes"], rows, cols, k, p0["scales"], p0["lut"])
+        _FULL[key] = (p0, wb)
+    p0, wb = _FULL[key]
+    x = synth.activations(seed + 100 * M, M, cols if axis == 1 else rows)
+    return p0, wb, x
+
+
+@pytest.mark.parametrize("M", [8, 16, 32])
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_prefill_agrees_with_its_own_oracle_full_size(orc, M, k):
+    """The tensor-core prefill (tcgen05, fp32 accumulation in tensor memory)
+    at 17408 x 5120: every bf16 output within the tolerance and equal to
+    bf16(y) of the oracle on at least 99% of the elements, where the
+    unrounded contract's output differs from it on at least 20% (checked on
+    1024 of the rows).  A dropped K chunk or a precision loss in the
+    accumulation fails the 99% even where the tolerance would pass."""
+    rows, cols = 17408, 5120
+    p, wb, x = _full_size(orc, 1, k, M, seed=51)
+    g = tcq.geometry(1, rows, cols, k)
+    got = host_bf16(tcq.trellis_prefill(dev(x), dev(p["codes"]), dev(p["scales"]), dev(p["lut"]), g))
+    y, a, out = orc.matmul_axis1(x, wb)
+    check_close(orc, got, y, a, f"prefill full M={M} k={k}")
+    agree = np.mean(got == out)
+    assert agree >= AGREE, f"prefill M={M} k={k}: bf16 equal to the oracle on {agree:.4f}"
+    sel = np.arange(0, rows, rows // 1024)[:1024]
+    w32 = orc.expand_f32(p["codes"][sel], len(sel), cols, k, p["scales"][sel], p["lut"])
+    _, _, out_unr = orc.matmul_axis1_f32w(x, w32)
+    assert np.mean(out_unr != out[:, sel]) >= DISAGREE
+
+
+@pytest.mark.parametrize("M", [4, 16, 32])
+def test_scatter_tensor_path_agrees_with_its_own_oracle_full_size(orc, M):
+    """The rounded axis-0 scatter from 3 activation rows (tensor cores) at
+    17408 x 5120, k=3, 128 splits, held to the same 99% agreement with the
+    oracle's bf16(y), with the unrounded contract differing on >= 20%
+    (checked on the first 2048 of the input rows)."""
+    rows, cols, k = 17408, 5120, 3
+    p, wb, x = _full_size(orc, 0, k, M, seed=53)
+    g = tcq.geometry(0, rows, cols, k)
+    got = host_bf16(tcq.trellis_scatter(dev(x), dev(p["codes"]), dev(p["scales"]), dev(p["lut"]), g, splits=128))
+    y, a, out, _ = orc.matmul_axis0(x, wb)
+    check_close(orc, got, y, a, f"scatter tensor path full M={M}")
+    agree = np.mean(got == out)
+    assert agree >= AGREE, f"scatter M={M}: bf16 equal to the oracle on {agree:.4f}"
+    n = 2048
+    w32 = orc.expand_f32(p["codes"][:n], n, cols, k, p["scales"][:n], p["lut"])
+    _, _, out_unr, _ = orc.matmul_axis0_f32w(x[:, :n], w32)
+    _, _, out_rnd, _ = orc.matmul_axis0(x[:, :n], wb[:n])
+    assert np.mean(out_unr != out_rnd) >= DISAGREE
+
+
 def test_unrounded_refused_where_the_operands_are_bf16():
     p = synth.problem(1, 8, 256, 512, 3, seed=25)
     d = _device(p)

@@ -79,7 +79,26 @@ trellis_status launched(cudaError_t e) {
     return TRELLIS_OK;
 }
 
-int resolve_splits(int32_t splits) { return splits == 0 ? 128 : splits; }
+// Split count of the scatter.  An explicit count is taken as given.  The
+// default is 128 for up to 4 activation rows (scatter.ts, SCATTER_SPLITS);
+// from 5 rows it is the rule of the split-K launcher (splitk-prefill.ts):
+// tiles of 32 activation rows and 32 output columns, 16-row K tiles,
+// ratio = max(1, floor(K tiles / (row tiles * column tiles))) and
+// splits = min(32, max(2, the power of two at or above ratio)).  At 17408 x
+// 5120 that is 8.  The rows of split s are [s*rp, min(rows, (s+1)*rp)) with
+// rp = ceil(rows/splits) for every count.
+int resolve_splits(const trellis_geometry* g, int32_t M, int32_t splits) {
+    if (splits != 0) return splits;
+    if (M <= 4) return 128;
+    const int64_t tiles_m = (M + 31) / 32;
+    const int64_t tiles_n = (g->cols + 31) / 32;
+    const int64_t tiles_k = g->rows / 16;
+    int64_t ratio = tiles_k / (tiles_m * tiles_n);
+    if (ratio < 1) ratio = 1;
+    int64_t p2 = 1;
+    while (p2 < ratio) p2 <<= 1;
+    return (int)(p2 < 2 ? 2 : p2 > 32 ? 32 : p2);
+}
 
 }  // namespace
 
@@ -134,7 +153,7 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
 
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {
     if (check_geometry(g, -1, true) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
-    return (size_t)M * (size_t)resolve_splits(splits) * (size_t)g->cols * sizeof(float);
+    return (size_t)M * (size_t)resolve_splits(g, M, splits) * (size_t)g->cols * sizeof(float);
 }
 
 trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
@@ -146,7 +165,7 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
     trellis_status st = check_geometry(g, 0, true);
     if (st != TRELLIS_OK) return st;
     if (M < 1 || M > 32 || splits < 0 || splits > 1024) return TRELLIS_ERR_SHAPE;
-    const int s = resolve_splits(splits);
+    const int s = resolve_splits(g, M, splits);
     if (!aligned16(x) || !aligned16(codes) || !aligned16(lut) || !aligned16(workspace) ||
         !aligned16(out))
         return TRELLIS_ERR_ALIGN;

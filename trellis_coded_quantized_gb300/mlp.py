@@ -105,8 +105,14 @@ class PackedMLPStack:
                          "out": out.clone()})
         return out
 
-    def forward(self, x, layers: int | None = None, keep=None):
-        """All layers (or the first `layers`) on x [M, hidden]; returns the last output."""
+    def forward(self, x, layers: int | None = None, keep=None, check: bool = True):
+        """All layers (or the first `layers`) on x [M, hidden]; returns the last output.
+
+        With `check` the pass ends by reading the library's device status
+        (which synchronises the device) and raises when a kernel's bounded
+        wait gave up: that kernel skipped its output, so the rows of every
+        later layer would be undefined.  Timed loops and CUDA-graph capture
+        pass check=False and read the status once afterwards."""
         M = x.shape[0]
         assert 1 <= M <= self.m_max
         cur = x
@@ -115,4 +121,9 @@ class PackedMLPStack:
             nxt = self.xs[l % 2][:M]
             self.layer(l, cur, nxt, keep)
             cur = nxt
+        if check:
+            status = tcq.trellis_device_status()
+            if status != 0:
+                raise RuntimeError(f"a kernel of the MLP pass gave up a bounded wait (device status {status}); "
+                                   "the pass output is undefined")
         return cur
