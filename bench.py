@@ -271,9 +271,13 @@ class Workload:
         elif w == "scatter":
             self.splits = cf["splits"]
             nt = 1 if self.M <= 8 else 2 if self.M <= 16 else 4
-            self.kernel = ("scatter_kernel<3> + split_reduce_kernel" if self.M <= 2 else
-                           f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel")
-            self.kernel_file = "scatter.cu"
+            if self.M <= 2:
+                self.kernel = "scatter_kernel<3> + split_reduce_kernel"
+            elif self.unrounded:
+                self.kernel = f"scatter_mma_kernel<3,{nt}> + split_reduce_kernel"
+            else:
+                self.kernel = f"scatter_tc_kernel<3,{16 if self.M <= 16 else 32}> + tc_split_reduce_kernel"
+            self.kernel_file = "scatter_tc.cu" if self.M >= 3 and not self.unrounded else "scatter.cu"
         else:
             raise ValueError(w)
         rows, cols = (self.N, self.K) if self.axis == 1 else (self.K, self.N)
@@ -286,7 +290,7 @@ class Workload:
         self.nsets = max(2, int(np.ceil(4 * l2 / self.packed)) + 1)
         self.sets = xor_sets(torch, codes0, self.nsets, 0x9E3779B9)
         self.g = tcq.geometry(self.axis, rows, cols, self.k, unrounded=self.unrounded)
-        if self.unrounded:
+        if self.unrounded and "(unrounded)" not in self.kernel:
             self.kernel += " (unrounded)"
         nout = rows if self.axis == 1 else cols
         self.out = torch.empty((self.M, nout), dtype=torch.bfloat16, device=device)

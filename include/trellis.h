@@ -2,7 +2,7 @@
  * trellis.h -- C ABI of libtrellis: the packed trellis-coded weight matmul on
  * one NVIDIA GB300 GPU (sm_103a).
  *
- * The method (pages: @mlx-bun/inference 1.0.0 diff, kernels/trellis/*.ts).
+ * The method (pages: @mlx-bun/inference 1.0.0 diff, the kernels/trellis TypeScript files).
  * A weight matrix of `rows` x `cols` is stored only as packed codes: each row
  * is cut into blocks of BT = 256 columns, and each block is a circular
  * bitstring of BT*k bits (k = 2, 3 or 4 bits per symbol) held in
@@ -20,8 +20,8 @@
  *     patterns (uint16), row-major.  The caller owns and allocates every
  *     buffer, inputs, outputs and workspace; the library allocates no memory
  *     and keeps no pointer after the call returns.  One exception:
- *     trellis_scatter_noalloc keeps its split partials in a fixed 16 MiB
- *     device array that the library itself declares (see there).
+ *     trellis_scatter_noalloc keeps its scratch in a fixed 21 MiB device
+ *     array that the library itself declares (see there).
  *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  Work is
  *     only enqueued: the call never synchronises.  Results are valid once
  *     the stream has reached the work.
@@ -173,14 +173,38 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
                                void* out, void* stream);
 
 /*
+ * trellis_scatter with the split sums left unrounded: out is f32 [M, cols],
+ * out[m][c] = sum over the splits of P[m][s][c], in the same order as
+ * trellis_scatter, which rounds exactly this value to bf16.  For a caller
+ * that still adds other partial sums before the rounding -- the rows of the
+ * same matrix held by other GPUs (the split-K sum over splits of scatter.ts
+ * and splitk-prefill.ts, continued across devices): all-reduce the f32
+ * outputs, then trellis_round_bf16.  Same arguments, rules and workspace as
+ * trellis_scatter; out must be 16-byte aligned.
+ */
+trellis_status trellis_scatter_f32(const void* x, int32_t M, const uint32_t* codes,
+                                   const void* scales, const float* lut,
+                                   const trellis_geometry* g, int32_t splits,
+                                   float* workspace, size_t workspace_bytes,
+                                   float* out, void* stream);
+
+/*
+ * out[i] = bf16( in[i] ), round to nearest even: the output rounding of the
+ * packed matmul (tiled-prefill.ts and scatter.ts, the final cast to T), for
+ * sums finished outside the library.  in f32 [n], out bf16 [n], n >= 1.
+ */
+trellis_status trellis_round_bf16(const float* in, int64_t n, void* out, void* stream);
+
+/*
  * trellis_scatter without a caller-provided workspace.  The pages have no
  * counterpart: this exists for callers that cannot allocate device memory,
  * such as plugin interfaces that pass in only input and output buffers, or
  * serving loops that must not call cudaMalloc because it can synchronise the
  * device.  Same arguments and result as trellis_scatter minus the workspace;
- * the fp32 split partials go to a 16 MiB array of device memory that the
- * library declares itself (reserved on every GPU that loads the library
- * until the process exits).
+ * the fp32 split partials (and the fix-up slots of the tensor-core path) go
+ * to a 21 MiB array of device memory that the library declares itself: 16
+ * MiB of partials and 5 MiB of fix-up space (reserved on every GPU that
+ * uses it until the process exits).
  *   - x and out must be 16-byte aligned, as for trellis_scatter;
  *   - M * splits * cols must be at most 4,194,304 (splits 0 is resolved as
  *     for trellis_scatter), else TRELLIS_ERR_WORKSPACE and nothing is
@@ -201,10 +225,15 @@ trellis_status trellis_scatter_noalloc(const void* x, int32_t M, const uint32_t*
                                        void* out, void* stream);
 
 /*
- * Bytes of workspace trellis_scatter needs: the fp32 partials
- * [M, splits, cols] of the scatter launch (scatter.ts, the [M, SPLITS, C]
- * float partial output), M * splits * cols * 4, with splits 0 resolved as
- * trellis_scatter does.  0 for invalid arguments.
+ * Bytes of workspace trellis_scatter needs, with splits 0 resolved as
+ * trellis_scatter does; 0 for invalid arguments:
+ *   - the fp32 partials [M, splits, cols] of the scatter launch (scatter.ts,
+ *     the [M, SPLITS, C] float partial output): M * splits * cols * 4;
+ *   - from 3 activation rows under the rounded contract (the tensor-core
+ *     path), after them, fix-up slots for the split reduction: 160 * M * 256
+ *     floats, M * 163840 bytes.  Its CTAs take equal runs of 16-row K steps
+ *     across the splits; a CTA that starts inside a split leaves its share of
+ *     that split's partial in its slot.
  */
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits);
 

@@ -102,10 +102,18 @@ def test_misaligned(lib):
     assert lib.trellis_scatter(_p(A), 1, _p(A), _p(A), _p(A), ctypes.byref(g0), 0, _p(U), 1 << 30, _p(A), None) == ALIGN
 
 
+def _fix(M, unrounded=False):
+    """Bytes of the tensor-core scatter's fix-up slots (3+ rows, rounded)."""
+    return 160 * M * 256 * 4 if M >= 3 and not unrounded else 0
+
+
 def test_workspace_size(lib):
     g0 = geometry(0, 17408, 5120, 3)
     assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 1, 0) == 1 * 128 * 5120 * 4
-    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 64) == 4 * 64 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 2, 0) == 2 * 128 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 64) == 4 * 64 * 5120 * 4 + _fix(4)
+    gu = geometry(0, 17408, 5120, 3, unrounded=True)
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(gu), 4, 64) == 4 * 64 * 5120 * 4
     assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 0, 0) == 0
     bad = geometry(0, 17408, 5000, 3)
     assert lib.trellis_scatter_workspace_bytes(ctypes.byref(bad), 1, 0) == 0
@@ -119,10 +127,11 @@ def test_default_split_count(lib):
     import pins
     for rows, cols, M, want in pins.read_default_splits():
         g0 = geometry(0, rows, cols, 3)
-        assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), M, 0) == M * want * cols * 4, (rows, cols, M)
+        assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), M, 0) == M * want * cols * 4 + _fix(M), \
+            (rows, cols, M)
     g0 = geometry(0, 17408, 5120, 3)
-    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 0) == 4 * 128 * 5120 * 4
-    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 8, 0) == 8 * 8 * 5120 * 4
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 0) == 4 * 128 * 5120 * 4 + _fix(4)
+    assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 8, 0) == 8 * 8 * 5120 * 4 + _fix(8)
 
 
 def test_glue_validation(lib):

@@ -2,7 +2,7 @@
 allocate device memory (for example plugin interfaces that hand a kernel only
 its input and output buffers, or serving loops where cudaMalloc's implicit
 device synchronisation is not allowed).  Its split partials live in the
-library's own 16 MiB device array instead of a caller workspace.
+library's own 21 MiB device array instead of a caller workspace.
 
 Checked through the C ABI against the ordinary trellis_scatter (which gets a
 workspace from the caller) and against the oracle's tolerance, on two calls in
@@ -55,7 +55,7 @@ def test_noalloc_rejects_partials_beyond_its_array():
     p = synth.problem(0, 32, rows, cols, k, seed=3)
     d = on_device(p)
     out = torch.empty((32, cols), dtype=torch.bfloat16, device="cuda")
-    # 32 * 128 * 5120 floats is more than the 4,194,304 the array holds
+    # 32 * 128 * 5120 floats is more than the 4,194,304 partials the array holds
     with pytest.raises(tcq.TrellisError, match="WORKSPACE"):
         tcq.trellis_scatter_noalloc(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128, out=out)
     # 6 * 128 * 5120 = 3,932,160 fits

@@ -162,10 +162,41 @@ def trellis_scatter(x, codes, scales, lut, g, splits: int = 0, workspace=None, o
     return out
 
 
+def trellis_scatter_f32(x, codes, scales, lut, g, splits: int = 0, workspace=None, out=None, stream=None):
+    """trellis_scatter with the split sums left in f32: x bf16 [M, rows] ->
+    out float32 [M, cols], not rounded (to be summed with other devices'
+    partial sums, then rounded by trellis_round_bf16)."""
+    torch = _torch()
+    c, s, t = _packed(codes, scales, lut, g)
+    M = x.shape[0]
+    xp = _dev(x, "x", _bf16_types(), (M, g.rows))
+    need = trellis_scatter_workspace_bytes(g, M, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4) // 4, dtype=torch.float32, device=x.device)
+    wp = _dev(workspace, "workspace", (torch.float32,))
+    if out is None:
+        out = torch.empty((M, g.cols), dtype=torch.float32, device=x.device)
+    op = _dev(out, "out", (torch.float32,), (M, g.cols))
+    _check(_lib.load().trellis_scatter_f32(xp, M, c, s, t, ctypes.byref(g), splits, wp,
+                                           workspace.numel() * 4, op, _stream(stream)), "trellis_scatter_f32")
+    return out
+
+
+def trellis_round_bf16(x, out=None, stream=None):
+    """float32 tensor -> bf16 tensor of the same shape, round to nearest even."""
+    torch = _torch()
+    xp = _dev(x, "x", (torch.float32,))
+    out = _out(out, tuple(x.shape), x)
+    op = _dev(out, "out", _bf16_types(), tuple(x.shape))
+    _check(_lib.load().trellis_round_bf16(xp, x.numel(), op, _stream(stream)), "trellis_round_bf16")
+    return out
+
+
 def trellis_scatter_noalloc(x, codes, scales, lut, g, splits: int = 0, out=None, stream=None):
     """Axis 0 like trellis_scatter, for callers that cannot allocate device
-    memory: the split partials live in the library's own 16 MiB device array,
-    so M * splits * cols may be at most 4,194,304.  Allocates nothing when
+    memory: the split partials live in the library's own 21 MiB device array
+    (16 MiB of partials, 5 MiB of fix-up slots), so M * splits * cols may be
+    at most 4,194,304.  Allocates nothing when
     `out` is given.  Calls that overlap on the GPU share that array and race."""
     c, s, t = _packed(codes, scales, lut, g)
     M = x.shape[0]

@@ -11,7 +11,8 @@ LIB_PATH = os.path.join(HERE, "libtrellis.so")
 
 # the entry points declared in include/trellis.h
 EXPORTS = (
-    "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_noalloc",
+    "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_f32",
+    "trellis_round_bf16", "trellis_scatter_noalloc",
     "trellis_scatter_workspace_bytes",
     "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_gather_probe",
     "trellis_device_status", "trellis_strerror",
@@ -33,6 +34,33 @@ _lock = threading.Lock()
 _lib = None
 
 
+def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures of the entry points on a loaded library."""
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    G = ctypes.POINTER(Geometry)
+    sig = {
+        "trellis_matvec": ([P, P, P, P, G, P, P], I32),
+        "trellis_gate_up_matvec": ([P, P, P, P, P, P, G, P, P], I32),
+        "trellis_prefill": ([P, I32, P, P, P, G, P, P], I32),
+        "trellis_scatter": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
+        "trellis_scatter_f32": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
+        "trellis_round_bf16": ([P, I64, P, P], I32),
+        "trellis_scatter_noalloc": ([P, I32, P, P, P, G, I32, P, P], I32),
+        "trellis_scatter_workspace_bytes": ([G, I32, I32], SZ),
+        "trellis_expand": ([P, P, P, G, P, P, P], I32),
+        "trellis_rmsnorm": ([P, I64, I64, ctypes.c_float, P, P], I32),
+        "trellis_silu_mul": ([P, P, I64, P, P], I32),
+        "trellis_gather_probe": ([P, I32, I32, I32, P, P], I32),
+        "trellis_device_status": ([ctypes.POINTER(I32)], I32),
+        "trellis_strerror": ([I32], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load libtrellis.so and declare its signatures; raises if it is missing."""
     global _lib
@@ -41,26 +69,5 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             return _lib
         if not os.path.exists(path):
             raise ImportError(f"libtrellis is not built ({path} missing): run __graft_entry__.build()")
-        lib = ctypes.CDLL(path)
-        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        G = ctypes.POINTER(Geometry)
-        sig = {
-            "trellis_matvec": ([P, P, P, P, G, P, P], I32),
-            "trellis_gate_up_matvec": ([P, P, P, P, P, P, G, P, P], I32),
-            "trellis_prefill": ([P, I32, P, P, P, G, P, P], I32),
-            "trellis_scatter": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
-            "trellis_scatter_noalloc": ([P, I32, P, P, P, G, I32, P, P], I32),
-            "trellis_scatter_workspace_bytes": ([G, I32, I32], SZ),
-            "trellis_expand": ([P, P, P, G, P, P, P], I32),
-            "trellis_rmsnorm": ([P, I64, I64, ctypes.c_float, P, P], I32),
-            "trellis_silu_mul": ([P, P, I64, P, P], I32),
-            "trellis_gather_probe": ([P, I32, I32, I32, P, P], I32),
-            "trellis_device_status": ([ctypes.POINTER(I32)], I32),
-            "trellis_strerror": ([I32], ctypes.c_char_p),
-        }
-        for name, (args, res) in sig.items():
-            f = getattr(lib, name)
-            f.argtypes = args
-            f.restype = res
-        _lib = lib
-        return lib
+        _lib = bind(ctypes.CDLL(path))
+        return _lib

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libtrellis.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["abi.cu", "expand.cu", "matvec.cu", "scatter.cu", "prefill.cu", "glue.cu"]
+SOURCES = ["abi.cu", "expand.cu", "matvec.cu", "scatter.cu", "scatter_tc.cu", "prefill.cu", "glue.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", INCLUDE, "-I", CSRC]
@@ -46,9 +46,9 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, out_dir: str = BUILD_DIR, defines=()) -> tuple[str, str]:
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -76,6 +76,32 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+# A second build of the same sources for the failure-path test only: the
+# prefill's code loader can withhold one mbarrier arrival (set through the
+# extra export trellis_test_set_withhold) and every bounded wait gives up
+# after 50 ms instead of 1 s.  Never loaded by the package.
+TEST_HOOKS_DIR = os.path.join(BUILD_DIR, "testhooks")
+TEST_HOOKS_LIB = os.path.join(TEST_HOOKS_DIR, "libtrellis_testhooks.so")
+TEST_HOOKS_DEFINES = ("-DTCQ_TEST_HOOKS", "-DTCQ_WAIT_LIMIT_NS=50000000ull")
+
+
+def build_test_hooks(force: bool = False) -> str:
+    """Compile and link the test-hooks variant of the library into _build/."""
+    if not force and os.path.exists(TEST_HOOKS_LIB) and \
+            all(os.path.getmtime(f) <= os.path.getmtime(TEST_HOOKS_LIB) for f in _deps()):
+        return TEST_HOOKS_LIB
+    os.makedirs(TEST_HOOKS_DIR, exist_ok=True)
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(lambda s: _compile(s, False, TEST_HOOKS_DIR, TEST_HOOKS_DEFINES), SOURCES))
+    tmp = TEST_HOOKS_LIB + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", *[o for o, _ in results], "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, TEST_HOOKS_LIB)
+    return TEST_HOOKS_LIB
 
 
 if __name__ == "__main__":

@@ -79,25 +79,26 @@ trellis_status launched(cudaError_t e) {
     return TRELLIS_OK;
 }
 
-// Split count of the scatter.  An explicit count is taken as given.  The
-// default is 128 for up to 4 activation rows (scatter.ts, SCATTER_SPLITS);
-// from 5 rows it is the rule of the split-K launcher (splitk-prefill.ts):
-// tiles of 32 activation rows and 32 output columns, 16-row K tiles,
-// ratio = max(1, floor(K tiles / (row tiles * column tiles))) and
-// splits = min(32, max(2, the power of two at or above ratio)).  At 17408 x
-// 5120 that is 8.  The rows of split s are [s*rp, min(rows, (s+1)*rp)) with
-// rp = ceil(rows/splits) for every count.
-int resolve_splits(const trellis_geometry* g, int32_t M, int32_t splits) {
-    if (splits != 0) return splits;
-    if (M <= 4) return 128;
-    const int64_t tiles_m = (M + 31) / 32;
-    const int64_t tiles_n = (g->cols + 31) / 32;
-    const int64_t tiles_k = g->rows / 16;
-    int64_t ratio = tiles_k / (tiles_m * tiles_n);
-    if (ratio < 1) ratio = 1;
-    int64_t p2 = 1;
-    while (p2 < ratio) p2 <<= 1;
-    return (int)(p2 < 2 ? 2 : p2 > 32 ? 32 : p2);
+// The checks and the launch shared by trellis_scatter and trellis_scatter_f32.
+trellis_status scatter_common(const void* x, int32_t M, const uint32_t* codes, const void* scales,
+                              const float* lut, const trellis_geometry* g, int32_t splits, float* workspace,
+                              size_t workspace_bytes, void* out, bool out_f32, void* stream) {
+    if (!x || !codes || !scales || !lut || !g || !out || !workspace) return TRELLIS_ERR_NULL;
+    trellis_status st = check_geometry(g, 0, true);
+    if (st != TRELLIS_OK) return st;
+    if (M < 1 || M > 32 || splits < 0 || splits > 1024) return TRELLIS_ERR_SHAPE;
+    const int s = tcq::scatter_splits(g->rows, g->cols, M, splits);
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(lut) || !aligned16(workspace) ||
+        !aligned16(out))
+        return TRELLIS_ERR_ALIGN;
+    if (workspace_bytes < trellis_scatter_workspace_bytes(g, M, splits)) return TRELLIS_ERR_WORKSPACE;
+    const DeviceFacts* d;
+    if ((st = current_device(&d)) != TRELLIS_OK) return st;
+    // the fix-up slots of the tensor-core path follow the partials
+    float* fix = workspace + (int64_t)M * s * g->cols;
+    return launched(tcq::launch_scatter(packed(codes, scales, lut, g), static_cast<const uint16_t*>(x), M, s,
+                                        workspace, fix, out, out_f32, d->status, d->sm_count,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -153,7 +154,9 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
 
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {
     if (check_geometry(g, -1, true) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
-    return (size_t)M * (size_t)resolve_splits(g, M, splits) * (size_t)g->cols * sizeof(float);
+    const bool unr = (g->flags & TRELLIS_FLAG_UNROUNDED) != 0;
+    return ((size_t)M * (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits) * (size_t)g->cols +
+            (size_t)tcq::scatter_fix_floats(M, unr)) * sizeof(float);
 }
 
 trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
@@ -161,20 +164,24 @@ trellis_status trellis_scatter(const void* x, int32_t M, const uint32_t* codes,
                                const trellis_geometry* g, int32_t splits,
                                float* workspace, size_t workspace_bytes,
                                void* out, void* stream) {
-    if (!x || !codes || !scales || !lut || !g || !out || !workspace) return TRELLIS_ERR_NULL;
-    trellis_status st = check_geometry(g, 0, true);
-    if (st != TRELLIS_OK) return st;
-    if (M < 1 || M > 32 || splits < 0 || splits > 1024) return TRELLIS_ERR_SHAPE;
-    const int s = resolve_splits(g, M, splits);
-    if (!aligned16(x) || !aligned16(codes) || !aligned16(lut) || !aligned16(workspace) ||
-        !aligned16(out))
-        return TRELLIS_ERR_ALIGN;
-    if (workspace_bytes < trellis_scatter_workspace_bytes(g, M, splits)) return TRELLIS_ERR_WORKSPACE;
+    return scatter_common(x, M, codes, scales, lut, g, splits, workspace, workspace_bytes, out, false, stream);
+}
+
+trellis_status trellis_scatter_f32(const void* x, int32_t M, const uint32_t* codes,
+                                   const void* scales, const float* lut,
+                                   const trellis_geometry* g, int32_t splits,
+                                   float* workspace, size_t workspace_bytes,
+                                   float* out, void* stream) {
+    return scatter_common(x, M, codes, scales, lut, g, splits, workspace, workspace_bytes, out, true, stream);
+}
+
+trellis_status trellis_round_bf16(const float* in, int64_t n, void* out, void* stream) {
+    if (!in || !out) return TRELLIS_ERR_NULL;
+    if (n < 1) return TRELLIS_ERR_SHAPE;
     const DeviceFacts* d;
+    trellis_status st;
     if ((st = current_device(&d)) != TRELLIS_OK) return st;
-    return launched(tcq::launch_scatter(packed(codes, scales, lut, g), static_cast<const uint16_t*>(x), M, s,
-                                        workspace, static_cast<uint16_t*>(out), d->sm_count,
-                                        static_cast<cudaStream_t>(stream)));
+    return launched(tcq::launch_round_bf16(in, n, static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
 }
 
 trellis_status trellis_expand(const uint32_t* codes, const void* scales, const float* lut,

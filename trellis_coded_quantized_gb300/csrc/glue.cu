@@ -31,6 +31,15 @@ rmsnorm_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* _
         orow[d] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(xr[d]) * inv));
 }
 
+// out[i] = bf16_rn(in[i]): the output rounding of the packed matmul, for a
+// sum that was finished outside the library (an all-reduce across GPUs).
+__global__ void round_bf16_kernel(const float* __restrict__ in, int64_t n, uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_release();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(in[i]));
+}
+
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                 int64_t n, uint16_t* __restrict__ out) {
     pdl_wait();
@@ -89,6 +98,15 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     const cudaError_t e = launch_pdl(silu_mul_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, g, u, n, out);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    const cudaError_t e = launch_pdl(round_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, in, n, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

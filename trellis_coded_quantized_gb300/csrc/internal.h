@@ -35,18 +35,61 @@ cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* 
                            int* status, int sm_count, cudaStream_t stream);
 
 // axis 0: partials [M, splits, cols] then the split reduction into out [M, cols]
+// out is bf16 [M, cols], or with out_f32 the unrounded f32 sums [M, cols]
 cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
-                           float* partial, uint16_t* out, int sm_count, cudaStream_t stream);
+                           float* partial, float* fix, void* out, bool out_f32, int* status, int sm_count,
+                           cudaStream_t stream);
+
+// axis 0 on the tensor cores (rounded contract, 3..32 rows): partials
+// [M, splits, cols] and fix-up slots fix [kScatterTcMaxCtas, M, 256], then
+// the split reduction
+cudaError_t launch_scatter_tc(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
+                              float* fix, void* out, bool out_f32, int* status, int sm_count,
+                              cudaStream_t stream);
+
+// Most CTAs of the tensor-core scatter (its fix-up space is sized for them;
+// GB300 has 152 SMs).
+constexpr int kScatterTcMaxCtas = 160;
+// Fewest activation rows that take the tensor-core scatter.
+constexpr int kScatterTcMinRows = 3;
+// Whether a scatter call takes the tensor-core path (and its fix-up space).
+inline bool scatter_uses_tc(int M, bool unrounded) { return !unrounded && M >= kScatterTcMinRows; }
+// Floats of fix-up space the scatter needs besides the partials.
+inline int64_t scatter_fix_floats(int M, bool unrounded) {
+    return scatter_uses_tc(M, unrounded) ? (int64_t)kScatterTcMaxCtas * M * 256 : 0;
+}
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t M, int64_t D, float eps,
                            uint16_t* out, cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n,
                             uint16_t* out, cudaStream_t stream);
+cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream);
 cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, int replicas, float* sink,
                                 cudaStream_t stream);
 
 // Largest input width the matvec kernel accepts (one 32-column unit per thread).
 constexpr int64_t kMatvecMaxCols = 640 * 32;
+
+// Split count of the scatter.  An explicit count is taken as given.  The
+// default is 128 for up to 4 activation rows (scatter.ts, SCATTER_SPLITS);
+// from 5 rows it is the rule of the split-K launcher (splitk-prefill.ts):
+// tiles of 32 activation rows and 32 output columns, 16-row K tiles,
+// ratio = max(1, floor(K tiles / (row tiles * column tiles))) and
+// splits = min(32, max(2, the power of two at or above ratio)).  At 17408 x
+// 5120 that is 8.  The rows of split s are [s*rp, min(rows, (s+1)*rp)) with
+// rp = ceil(rows/splits) for every count.
+inline int scatter_splits(int64_t rows, int64_t cols, int M, int splits) {
+    if (splits != 0) return splits;
+    if (M <= 4) return 128;
+    const int64_t tiles_m = (M + 31) / 32;
+    const int64_t tiles_n = (cols + 31) / 32;
+    const int64_t tiles_k = rows / 16;
+    int64_t ratio = tiles_k / (tiles_m * tiles_n);
+    if (ratio < 1) ratio = 1;
+    int64_t p2 = 1;
+    while (p2 < ratio) p2 <<= 1;
+    return (int)(p2 < 2 ? 2 : p2 > 32 ? 32 : p2);
+}
 
 // Status codes a kernel may record in the device status word.
 constexpr int kStatusWaitTimeout = 1;

@@ -66,7 +66,20 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator columns [256, 256 + N)
 // tensor-memory column of A stage st: [0, 128), [128, 256), [384, 512)
 __host__ __device__ constexpr uint32_t a_col(int st) { return st < 2 ? (uint32_t)st * 128u : 384u; }
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Wall-clock limit of every mbarrier wait (a test build of the library sets
+// a shorter one).
+#ifndef TCQ_WAIT_LIMIT_NS
+#define TCQ_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = TCQ_WAIT_LIMIT_NS;
+
+#ifdef TCQ_TEST_HOOKS
+// test build only (see trellis_test_set_withhold at the end of this file)
+__device__ int g_test_withhold;
+__device__ __forceinline__ bool test_withhold_arrival() {
+    return *reinterpret_cast<volatile int*>(&g_test_withhold) != 0;
+}
+#endif
 
 template <int K, int NPAD>
 struct PfLayout {
@@ -228,6 +241,12 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                              :: "r"(ct + r * Lay::kPitch + part * 16), "l"(src0 + (int64_t)r * wpr + part * 4)
                              : "memory");
             }
+#ifdef TCQ_TEST_HOOKS
+            // test build only: with the hook set, lane 0 of CTA 0 withholds its
+            // arrival for the first code tile, so the decoders' bounded wait on
+            // it runs out and the kernel takes its abort path
+            if (b == 0 && lane == 0 && blockIdx.x == 0 && test_withhold_arrival()) continue;
+#endif
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
                          :: "r"(tc::smem_addr(&cfull[cst])) : "memory");
         }
@@ -349,3 +368,13 @@ cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* 
 }
 
 }  // namespace tcq
+
+#ifdef TCQ_TEST_HOOKS
+// Test build only, not part of the C ABI: nonzero makes the prefill's code
+// loader withhold one mbarrier arrival (lane 0 of CTA 0, first code tile) so
+// that the decoders' bounded wait runs out.  Returns the cudaError_t of the
+// copy to the device flag.
+extern "C" int trellis_test_set_withhold(int on) {
+    return (int)cudaMemcpyToSymbol(tcq::g_test_withhold, &on, sizeof on);
+}
+#endif

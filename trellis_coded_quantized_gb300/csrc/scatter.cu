@@ -164,8 +164,9 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
 constexpr int kRdGroups = 32;
 constexpr int kRdCols = 32;
 
+template <bool F32OUT>
 __global__ void __launch_bounds__(256)
-split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16_t* __restrict__ out) {
+split_reduce_kernel(const float* __restrict__ partial, int splits, int C, void* __restrict__ out_) {
     __shared__ float4 red[kRdGroups][kRdCols / 4];
     // launched as a programmatic dependent of the scatter: wait until that
     // grid has completed and its partials are visible (a no-op otherwise)
@@ -191,12 +192,16 @@ split_reduce_kernel(const float* __restrict__ partial, int splits, int C, uint16
             const float4 v = red[g][threadIdx.x];
             t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&lo);
-        o.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + (int64_t)m * C + cq * 4) = o;
+        if constexpr (F32OUT) {
+            reinterpret_cast<float4*>(out_)[(int64_t)m * (C / 4) + cq] = t;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&lo);
+            o.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out_) + (int64_t)m * C + cq * 4) = o;
+        }
     }
 }
 
@@ -539,8 +544,11 @@ cudaError_t launch_mma(const Packed& p, const uint16_t* x, int M, int splits, fl
 constexpr int kMmaMinRows = TCQ_MMA_MIN_ROWS;
 
 cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
-                           float* partial, uint16_t* out, int sm_count, cudaStream_t stream) {
-    (void)sm_count;
+                           float* partial, float* fix, void* out, bool out_f32, int* status, int sm_count,
+                           cudaStream_t stream) {
+    // 3 and more activation rows, rounded contract: the tcgen05 kernel
+    if (scatter_uses_tc(M, p.unrounded))
+        return launch_scatter_tc(p, x, M, splits, partial, fix, out, out_f32, status, sm_count, stream);
     cudaError_t e;
     // up to 2 activation rows: FMA kernel, each decoded weight feeding every
     // row; 3 and more: one pass on the tensor cores (under the unrounded
@@ -559,8 +567,10 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     const int C = (int)p.cols;
     // programmatic dependent launch: the reduction's CTAs are placed while
     // the last scatter pass still runs and start reading when it completes
-    e = launch_pdl(split_reduce_kernel, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0, stream,
-                   static_cast<const float*>(partial), splits, C, out);
+    e = out_f32 ? launch_pdl(split_reduce_kernel<true>, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0,
+                             stream, static_cast<const float*>(partial), splits, C, out)
+                : launch_pdl(split_reduce_kernel<false>, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0,
+                             stream, static_cast<const float*>(partial), splits, C, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -574,10 +584,12 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
 // interface of an inference runtime that passes in only the input and output
 // buffers, or a serving loop that must not call cudaMalloc because it can
 // synchronise the device and stall every other stream.  This entry point
-// keeps the fp32 split partials in a fixed array in device memory that the
-// library itself declares, so the call needs no allocation at all.  The
-// array is created when the library is loaded onto a GPU and stays reserved
-// on every GPU that loads the library until the process exits.
+// keeps the fp32 split partials, and the fix-up slots of the tensor-core
+// path, in a fixed array in device memory that the library itself declares,
+// so the call needs no allocation at all.  The driver reserves the array
+// when the library's scatter code is first used on a GPU (lazy module
+// loading), and it stays reserved on every GPU that used it until the
+// process exits.
 // ---------------------------------------------------------------------------
 #include "trellis.h"
 
@@ -585,7 +597,11 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
 
 namespace {
 
-constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;   // 16 MiB
+// 16 MiB of partials (M * splits * cols <= 4,194,304), then 5 MiB for the
+// fix-up slots of the tensor-core path at up to 32 activation rows
+constexpr size_t kNoAllocPartialFloats = size_t(1) << 22;
+constexpr size_t kNoAllocScratchFloats =
+    kNoAllocPartialFloats + (size_t)tcq::kScatterTcMaxCtas * 32 * 256;
 static __device__ __align__(256) float g_scatter_scratch[kNoAllocScratchFloats];
 
 constexpr int kNoAllocMaxDevices = 64;
@@ -600,8 +616,11 @@ extern "C" trellis_status trellis_scatter_noalloc(const void* x, int32_t M, cons
                                                   const trellis_geometry* g, int32_t splits,
                                                   void* out, void* stream) {
     if (!g) return TRELLIS_ERR_NULL;
+    // invalid arguments give 0 here and are reported by trellis_scatter
     const size_t need = trellis_scatter_workspace_bytes(g, M, splits);
-    if (need > kNoAllocScratchFloats * sizeof(float)) return TRELLIS_ERR_WORKSPACE;
+    if (need > 0 && (size_t)M * (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits) * (size_t)g->cols >
+                        kNoAllocPartialFloats)
+        return TRELLIS_ERR_WORKSPACE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
         cudaGetLastError();
@@ -616,8 +635,10 @@ extern "C" trellis_status trellis_scatter_noalloc(const void* x, int32_t M, cons
         if (g_scratch_err[dev] != cudaSuccess) cudaGetLastError();
     });
     if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return TRELLIS_ERR_DEVICE;
-    // Every partial the reduction reads is written by this same call (empty
-    // splits store zeros), so nothing in the scratch has to be cleared first.
+    // Every partial and fix-up slot the reduction reads is written by this
+    // same call (empty splits store zeros), so nothing in the scratch has to
+    // be cleared first.  The partials fit the first 16 MiB, so the fix-up
+    // slots that trellis_scatter places right after them fit the array.
     return trellis_scatter(x, M, codes, scales, lut, g, splits, g_scratch_ptr[dev],
                            kNoAllocScratchFloats * sizeof(float), out, stream);
 }

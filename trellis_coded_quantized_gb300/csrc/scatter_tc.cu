@@ -1,0 +1,573 @@
+// trellis_scatter on the 5th-generation tensor cores (rounded contract,
+// 3..32 activation rows): out[m][c] = bf16(sum_r x[m][r] w[r][c]) through
+// fp32 split partials P[m][s][c] (@mlx-bun/inference 1.0.0,
+// kernels/trellis/scatter.ts: split ranges, the [M, SPLITS, C] float
+// partials and their sum over the split axis; splitk-prefill.ts computes the
+// same partials with 8x8 simdgroup MMAs on weights decoded into threadgroup
+// memory).
+//
+// The MMA is D[c][m] += W^T[c][r] X^T[r][m]: output columns are the MMA
+// rows (tensor-memory lanes), the input rows of the split are K, the
+// activation rows (padded to N = 16 or 32) are N.
+//   - A (decoded weights) is written straight into TENSOR MEMORY with the
+//     16x256b store shape, so the MMA reads only the small B operand from
+//     shared memory, where the codebook gathers already take the bandwidth.
+//     That shape fills 16 lanes of a warp's 32-lane quarter; the other 16
+//     lanes are left out, so an M = 128 MMA carries 64 output columns and a
+//     256-column block is four "regions" of 64 columns.  In a region a thread
+//     (g = lane / 4, c = lane % 4) of quarter q fills lanes 32q+g and
+//     32q+g+8 with K rows 4c..4c+3; it owns the 8 consecutive columns
+//     64q + 8g .. +7 of the block, region r holding columns 64q + 8g + 2r
+//     (lane 32q+g) and 64q + 8g + 2r + 1 (lane 32q+g+8).  The rows of D past
+//     lane 16 of a quarter are never read;
+//   - B (activations x[m][r0 .. r0+63]) is K-major with the 128-byte swizzle,
+//     copied by one loader warp with cp.async (zero rows past M and past the
+//     split) into a ring of 4 stages;
+//   - the code words of a stage (its rows of one block) are copied by a code
+//     loader warp with cp.async into a ring of 3 tiles of 128-byte rows, the
+//     16-byte chunks of row r rotated by 2 * ((r / 4) % 4) so that the four
+//     rows a warp reads at once sit in four different bank groups;
+//   - D (fp32) lives in tensor memory, two buffers of 4 regions x N columns,
+//     so the epilogue of one item overlaps the MMAs of the next.
+// A stage is up to 64 rows (4 K steps) of one item (one split, one block of
+// 256 columns).  Persistent CTAs, one per SM, take equal runs of K steps
+// over all items (splitk_schedule.cuh); a CTA that starts inside an item
+// leaves its share in a fix-up slot that the split reduction adds in CTA
+// order.
+//
+// Warps: 16 decoders (warp w: lane quarter w % 4, K step w / 4 of the stage;
+// a thread decodes 8 windows of each of its 4 rows from 3 words of the code
+// tile), 4 epilogue warps (lane quarters 0..3), 1 MMA warp, 1 activation
+// loader, 1 code loader.  Every mbarrier wait is bounded (1 s); a wait that
+// gives up sets the CTA's abort flag and the device status word, and the
+// kernel returns without further output.
+#include "common.cuh"
+#include "internal.h"
+#include "splitk_schedule.cuh"
+#include "tc.cuh"
+
+namespace tcq {
+namespace {
+
+constexpr int kStDecWarps = 16;                 // warps 16..19: epilogue, lane quarters 0..3
+constexpr int kStMmaWarp = 20;
+constexpr int kStActWarp = 21;
+constexpr int kStCodeWarp = 22;
+constexpr int kStThreads = 23 * 32;
+constexpr int kStRows = 64;                     // rows (K) of a stage: 4 MMA steps of 16
+constexpr int kStSteps = kStRows / 16;
+constexpr int kStStages = 2;                    // stages of decoded weights (A, tensor memory)
+constexpr int kStBStages = 4;                   // stages of activations (B)
+constexpr int kStCStages = 3;                   // stages of code tiles
+constexpr int kStPitch = 128;                   // bytes per row of a code tile
+constexpr int kStCBytes = kStRows * kStPitch;   // one code tile (8 KB)
+constexpr uint32_t kStTmemCols = 512;
+constexpr uint32_t kStACol = 256;               // A stages at [256, 512): 4 regions x 32 columns each
+constexpr uint64_t kStWaitNs = 1000000000ull;
+
+template <int NPAD>
+struct StLayout {
+    static constexpr int kB = NPAD * 128;       // activations of one stage: NPAD rows x 64 K
+    static constexpr int kBOff = 0;
+    static constexpr int kCOff = kBOff + kStBStages * kB;
+    static constexpr int kLutOff = kCOff + kStCStages * kStCBytes;
+    static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
+    // 32 mbarriers, the tensor-memory address and the abort flag
+    static constexpr int kBarBytes = 320;
+    static constexpr int kBytes = kBarOff + kBarBytes;
+    static constexpr int kAlloc = kBytes + 1024;    // slack for 1024-byte alignment
+};
+
+// One stage of the CTA's run: up to kStSteps steps of one item.
+struct Stage {
+    int s, b;          // split, block of 256 columns
+    int k, take, n;    // first step within the item, steps taken, steps of the item
+    int64_t r_begin;   // first input row
+    int valid;         // rows of the stage inside the split (<= 16 * take)
+    bool first;        // first stage of this item in the CTA
+    bool last;         // last stage of this item in the CTA
+};
+
+// Walks the CTA's run stage by stage.  Only the start is located by
+// division; after that the position advances by additions, so the per-stage
+// bookkeeping costs every thread a few instructions.
+struct Cursor {
+    int64_t x, xe;     // next step, end of the run
+    int s, b, k, n;    // item and step within it of x, steps of that item
+    bool fresh;        // no stage taken yet
+};
+
+__device__ __forceinline__ void cursor_init(const SplitSchedule& sc, Cursor& c, int64_t xb, int64_t xe) {
+    c.x = xb;
+    c.xe = xe;
+    c.s = c.b = c.k = c.n = 0;
+    if (xb < xe) sc.locate(xb, c.s, c.b, c.k, c.n);
+    c.fresh = true;
+}
+
+__device__ __forceinline__ bool next_stage(const SplitSchedule& sc, Cursor& c, Stage& st) {
+    if (c.x >= c.xe) return false;
+    st.s = c.s;
+    st.b = c.b;
+    st.k = c.k;
+    st.n = c.n;
+    int take = c.n - c.k;
+    if (take > kStSteps) take = kStSteps;
+    if ((int64_t)take > c.xe - c.x) take = (int)(c.xe - c.x);
+    st.take = take;
+    st.first = c.k == 0 || c.fresh;
+    st.last = c.k + take == c.n || c.x + take == c.xe;
+    st.r_begin = sc.row0(st.s) + 16 * (int64_t)st.k;
+    const int64_t v = sc.row1(st.s) - st.r_begin;
+    st.valid = (int)(v < 16 * take ? v : 16 * take);
+    c.fresh = false;
+    c.x += take;
+    c.k += take;
+    if (c.k == c.n) {                  // next item: next block, then next split
+        c.k = 0;
+        if (++c.b == sc.NB) {
+            c.b = 0;
+            ++c.s;
+            c.n = sc.steps(c.s);       // past the last non-empty split x has reached xe
+        }
+    }
+    return true;
+}
+
+// Byte offset of word w of row r in a code tile (16-byte chunks rotated by
+// 2 * ((r / 4) % 4) within the 128-byte row).
+__device__ __forceinline__ uint32_t ctile_off(int r, int w) {
+    return (uint32_t)r * kStPitch + ((((uint32_t)w >> 2) + 2u * (((uint32_t)r >> 2) & 3u)) & 7u) * 16u +
+           ((uint32_t)w & 3u) * 4u;
+}
+
+// tcgen05.st of 4 registers per thread in the 16x256b shape: thread (g, c)
+// writes lanes g and g+8 of the 16 lanes at taddr, columns 2c and 2c+1.
+__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(taddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
+template <int K, int NPAD>
+__global__ void __launch_bounds__(kStThreads, 1)
+scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
+                  const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+                  int C, int interleave, SplitSchedule sc, float* __restrict__ partial,
+                  float* __restrict__ fix, int* __restrict__ status) {
+    using Lay = StLayout<NPAD>;
+    extern __shared__ uint8_t smem_raw[];
+    // nothing is read, written or allocated before the previous kernel of
+    // the stream has completed
+    pdl_wait();
+    pdl_release();
+    uint8_t* base = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
+    float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
+    // afull[stage][step]: the 4 warps of one 16-row step wrote their part of
+    // A, so that step's 4 MMAs can go
+    uint64_t* afull = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);
+    uint64_t* aempty = afull + kStStages * kStSteps;                       // MMA done with A
+    uint64_t* bfull = aempty + kStStages;                                  // loader wrote B
+    uint64_t* bempty = bfull + kStBStages;                                 // MMA done with B
+    uint64_t* cfull = bempty + kStBStages;                                 // code tile landed
+    uint64_t* cempty = cfull + kStCStages;                                 // code tile read
+    uint64_t* dfull = cempty + kStCStages;                                 // an item's D complete
+    uint64_t* dempty = dfull + 2;                                          // epilogue done with D
+    uint64_t* done = dempty + 2;                                           // every MMA complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    static_assert((kStStages * kStSteps + kStStages + 2 * kStBStages + 2 * kStCStages + 5) * 8 + 8 <= Lay::kBarBytes,
+                  "barrier area too small");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    stage_lut_rep8(lut_s, lut);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStStages * kStSteps; ++i) tc::mbar_init(&afull[i], 4 * 32);
+        for (int i = 0; i < kStStages; ++i) tc::mbar_init(&aempty[i], 1);
+        for (int i = 0; i < kStBStages; ++i) {
+            tc::mbar_init(&bfull[i], 32);
+            tc::mbar_init(&bempty[i], 1);
+        }
+        for (int i = 0; i < kStCStages; ++i) {
+            tc::mbar_init(&cfull[i], 32);
+            tc::mbar_init(&cempty[i], kStDecWarps * 32);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&dfull[i], 1);
+            tc::mbar_init(&dempty[i], 4 * 32);
+        }
+        tc::mbar_init(done, 1);
+        *abort_flag = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == kStMmaWarp) {
+        tc::tmem_alloc(tmem_slot, kStTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t xb = sc.start(blockIdx.x), xe = sc.start(blockIdx.x + 1);
+    const uint32_t s_base = tc::smem_addr(base);
+    const uint32_t b_base = s_base + Lay::kBOff;
+    const uint32_t c_base = s_base + Lay::kCOff;
+    const int64_t R = sc.R;
+    constexpr int wpb = kBT * K / 32;
+
+    if (warp < kStDecWarps) {
+        // ------------------------------------------------------------ decoders
+        const int q = warp & 3, ks = warp >> 2;
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t gofs = lut_rep_lane_offset();
+        // columns t0 .. t0+7 of the block; the window of column t0+e starts at
+        // bit (255 - t0 - e) k = S + (7 - e) k, S = (248 - t0) k
+        const int t0 = 64 * q + 8 * g;
+        const int S = (248 - t0) * K;
+        const int wi = S >> 5;
+        const uint32_t off = (uint32_t)(S & 31);
+        const int w1i = wi + 1 < wpb ? wi + 1 : wi + 1 - wpb;
+        const int w2i = wi + 2 < wpb ? wi + 2 : wi + 2 - wpb;
+        // this thread's rows of the stage: 16 ks + 4c + i, i = 0..3
+        const int row0 = 16 * ks + 4 * c;
+        uint32_t woff[3];
+        woff[0] = ctile_off(row0, wi);
+        woff[1] = ctile_off(row0, w1i);
+        woff[2] = ctile_off(row0, w2i);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        Cursor cur;
+        cursor_init(sc, cur, xb, xe);
+        Stage st;
+        for (int j = 0; next_stage(sc, cur, st); ++j) {
+            const int as = j % kStStages, cs = j % kStCStages;
+            const bool active = ks < st.take;
+            uint32_t pk[16];
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[cs], (j / kStCStages) & 1, abort_flag, kStWaitNs)))
+                break;
+            if (active) {
+                // words and scales of the 4 rows, then the tile is released
+                uint32_t wv[4][3];
+                float sv[4];
+                const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool in = row0 + i < st.valid;
+                    #pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        uint32_t v;
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + woff[t] + (uint32_t)i * kStPitch));
+                        wv[i][t] = in ? v : 0u;
+                    }
+                    sv[i] = in ? bf16_bits_to_float(__ldg(scales + st.r_begin + row0 + i)) : 0.f;
+                }
+                tc::mbar_arrive(&cempty[cs]);
+                // bits [S, S + 64) of each row: the window of column t0+e at bit (7-e) k
+                uint32_t ww[4][2];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ww[i][0] = __funnelshift_r(wv[i][0], wv[i][1], off);
+                    ww[i][1] = __funnelshift_r(wv[i][1], wv[i][2], off);
+                }
+                // region r: lane g <- column t0+2r, lane g+8 <- column t0+2r+1;
+                // registers (rows 4c, 4c+1) and (rows 4c+2, 4c+3) of each
+                auto wgt = [&](int i, int e) {
+                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), sv[i]);
+                };
+                #pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    pk[4 * r + 0] = pack_bf16x2(wgt(0, 2 * r), wgt(1, 2 * r));
+                    pk[4 * r + 1] = pack_bf16x2(wgt(2, 2 * r), wgt(3, 2 * r));
+                    pk[4 * r + 2] = pack_bf16x2(wgt(0, 2 * r + 1), wgt(1, 2 * r + 1));
+                    pk[4 * r + 3] = pack_bf16x2(wgt(2, 2 * r + 1), wgt(3, 2 * r + 1));
+                }
+            } else {
+                tc::mbar_arrive(&cempty[cs]);
+            }
+            // the warp leaves together: a wait that gave up in one lane ends the loop in all
+            if (j >= kStStages &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&aempty[as], ((j / kStStages) - 1) & 1, abort_flag, kStWaitNs)))
+                break;
+            if (active) {
+                tc::tc_fence_after();
+                #pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    tmem_st_16x256b(lane_base + kStACol + (uint32_t)(as * 128 + r * 32 + ks * 8),
+                                    pk[4 * r + 0], pk[4 * r + 1], pk[4 * r + 2], pk[4 * r + 3]);
+                tc::tmem_wait_st();
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&afull[as * kStSteps + ks]);
+        }
+    } else if (warp == kStCodeWarp) {
+        // ------------------------------------------------------------ code loader
+        // The stage's rows of block b in 16-byte cp.async chunks (a warp
+        // instruction covers 4 to 2 rows), rotated within the 128-byte tile
+        // rows; each lane's copies arrive on cfull[cs] when they land.
+        const int64_t rs = block_row_stride(C / kBT, wpb, interleave);
+        constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
+        Cursor cur;
+        cursor_init(sc, cur, xb, xe);
+        Stage st;
+        for (int j = 0; next_stage(sc, cur, st); ++j) {
+            const int cs = j % kStCStages;
+            if (j >= kStCStages &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&cempty[cs], ((j / kStCStages) - 1) & 1, abort_flag, kStWaitNs)))
+                break;
+            const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
+            const uint32_t* src0 = codes + block_col_base(st.b, R, wpb, interleave) + st.r_begin * rs;
+            const int nchunks = st.valid * cpr;
+            for (int ch = lane; ch < nchunks; ch += 32) {
+                const int r = ch / cpr, part = ch - (ch / cpr) * cpr;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(tile + ctile_off(r, 4 * part)), "l"(src0 + (int64_t)r * rs + 4 * part)
+                             : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                         :: "r"(tc::smem_addr(&cfull[cs])) : "memory");
+        }
+    } else if (warp == kStActWarp) {
+        // ------------------------------------------------------------ activation loader
+        Cursor cur;
+        cursor_init(sc, cur, xb, xe);
+        Stage st;
+        for (int j = 0; next_stage(sc, cur, st); ++j) {
+            const int bs_i = j % kStBStages;
+            if (j >= kStBStages &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&bempty[bs_i], ((j / kStBStages) - 1) & 1, abort_flag, kStWaitNs)))
+                break;
+            const uint32_t bs = b_base + (uint32_t)bs_i * Lay::kB;
+            #pragma unroll 1
+            for (int idx = lane; idx < NPAD * 8; idx += 32) {
+                const int n = idx >> 3, c8 = idx & 7;
+                const uint32_t dst = bs + (uint32_t)n * 128u + ((uint32_t)(c8 ^ (n & 7)) << 4);
+                int cnt = st.valid - 8 * c8;
+                cnt = cnt < 0 ? 0 : cnt > 8 ? 8 : cnt;
+                const int64_t e = (int64_t)n * R + st.r_begin + 8 * c8;
+                if (n < M && cnt == 8 && (e & 7) == 0) {
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(x + e) : "memory");
+                } else if (n < M && cnt > 0) {
+                    uint32_t v[4];
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t lo = 2 * q < cnt ? (uint32_t)__ldg(x + e + 2 * q) : 0u;
+                        const uint32_t hi = 2 * q + 1 < cnt ? (uint32_t)__ldg(x + e + 2 * q + 1) : 0u;
+                        v[q] = lo | (hi << 16);
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 :: "r"(dst), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
+                } else {
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" :: "r"(dst), "l"(x) : "memory");
+                }
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&bfull[bs_i]);
+        }
+    } else if (warp == kStMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(128, NPAD);
+            Cursor cur;
+            cursor_init(sc, cur, xb, xe);
+            Stage st;
+            int ic = -1;
+            for (int j = 0; next_stage(sc, cur, st); ++j) {
+                if (st.first) {
+                    ++ic;
+                    if (ic >= 2 && !tc::mbar_wait(&dempty[ic & 1], ((ic >> 1) - 1) & 1, abort_flag, kStWaitNs))
+                        break;
+                }
+                const int as = j % kStStages, bs_i = j % kStBStages;
+                if (!tc::mbar_wait(&bfull[bs_i], (j / kStBStages) & 1, abort_flag, kStWaitNs)) break;
+                const uint32_t d = tmem + (uint32_t)(ic & 1) * (4 * NPAD);
+                const uint32_t bsa = b_base + (uint32_t)bs_i * Lay::kB;
+                // each 16-row step as soon as its four warps are done
+                bool ok = true;
+                for (int kk = 0; kk < st.take; ++kk) {
+                    if (!tc::mbar_wait(&afull[as * kStSteps + kk], (j / kStStages) & 1, abort_flag, kStWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint64_t bd = tc::sdesc_sw128(bsa + (uint32_t)kk * 32u, 1024u);
+                    #pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        tc::mma_ts(d + (uint32_t)r * NPAD, tmem + kStACol + (uint32_t)(as * 128 + r * 32 + kk * 8), bd,
+                                   idesc, (st.first && kk == 0) ? 0u : 1u);
+                }
+                if (!ok) break;
+                tc::mma_commit(&aempty[as]);
+                tc::mma_commit(&bempty[bs_i]);
+                if (st.last) tc::mma_commit(&dfull[ic & 1]);
+            }
+            tc::mma_commit(done);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int g = lane & 7, h = (lane >> 3) & 1;
+        Cursor cur;
+        cursor_init(sc, cur, xb, xe);
+        Stage st;
+        int ic = -1;
+        bool from_zero = false;
+        while (next_stage(sc, cur, st)) {
+            if (st.first) {
+                ++ic;
+                from_zero = st.k == 0;
+            }
+            if (!st.last) continue;
+            const int d = ic & 1;
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[d], (ic >> 1) & 1, abort_flag, kStWaitNs))) break;
+            tc::tc_fence_after();
+            // the CTA that holds the item's first step writes the partial
+            // itself; a CTA that starts inside an item (only ever its first
+            // item) writes its share to its own fix-up slot
+            float* dstb = from_zero ? partial + (int64_t)st.s * C + (int64_t)st.b * kBT
+                                    : fix + ((int64_t)blockIdx.x * M) * kBT;
+            const int64_t mstride = from_zero ? (int64_t)sc.S * C : (int64_t)kBT;
+            // 16 activation rows at a time
+            #pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+                #pragma unroll
+                for (int m0 = 0; m0 < NPAD; m0 += 16) {
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)d * (4 * NPAD) + (uint32_t)(r * NPAD + m0), v);
+                    tc::tmem_wait_ld();
+                    if (lane < 16) {           // lanes 16..31 of the quarter carry no column
+                        float* dst = dstb + 64 * q + 8 * g + 2 * r + h + m0 * mstride;
+                        #pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            if (m0 + m < M) *dst = __uint_as_float(v[m]);
+                            dst += mstride;
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&dempty[d]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == kStMmaWarp) {
+        // no MMA may still write tensor memory when it is released
+        tc::mbar_wait(done, 0, abort_flag, kStWaitNs);
+        __syncwarp();
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kStTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(status, kStatusWaitTimeout);
+}
+
+// out[m][c] = bf16( sum_s P[m][s][c] ).  The CTA that holds an item's first
+// step has written its share of P to the workspace; when the item runs on
+// into later CTAs, their fix-up slots are added to it here in CTA order and
+// the sum is stored back; P of an empty split is zero.  A CTA covers 32 columns of one activation
+// row with 32 groups of 8 threads; group g takes a contiguous run of splits
+// in order, then the 32 runs are added in order.
+template <bool F32OUT>
+__global__ void __launch_bounds__(256)
+tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fix, SplitSchedule sc,
+                       int M, int C, void* __restrict__ out_) {
+    __shared__ float4 red[32][8];
+    pdl_wait();
+    pdl_release();
+    const int m = blockIdx.y;
+    const int col = (blockIdx.x * 8 + (threadIdx.x & 7)) * 4;
+    const int b = col >> 8, cl = col & 255;
+    const int grp = threadIdx.x >> 3;
+    const int S = sc.S;
+    const int per = (S + 31) / 32;
+    const int s0 = grp * per, s1 = min(S, s0 + per);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = s0; s < s1; ++s) {
+        float4* pp = reinterpret_cast<float4*>(partial + ((int64_t)m * S + s) * C + col);
+        const int n = sc.steps(s);
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (n == 0) {
+            *pp = p;
+        } else {
+            const int64_t x0 = (int64_t)sc.NB * sc.prefix(s) + (int64_t)b * n;
+            const int g1 = sc.cta_of(x0), g2 = sc.cta_of(x0 + n - 1);
+            p = *pp;
+            if (g2 > g1) {
+                for (int g = g1 + 1; g <= g2; ++g) {
+                    if (sc.start(g) == sc.start(g + 1)) continue;     // a CTA with no steps
+                    const float4 v = *reinterpret_cast<const float4*>(fix + ((int64_t)g * M + m) * kBT + cl);
+                    p.x += v.x; p.y += v.y; p.z += v.z; p.w += v.w;
+                }
+                *pp = p;
+            }
+        }
+        a.x += p.x; a.y += p.y; a.z += p.z; a.w += p.w;
+    }
+    red[grp][threadIdx.x & 7] = a;
+    __syncthreads();
+    if (grp == 0) {
+        float4 t = red[0][threadIdx.x];
+        for (int g = 1; g < 32; ++g) {
+            const float4 v = red[g][threadIdx.x];
+            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+        }
+        if constexpr (F32OUT) {
+            *reinterpret_cast<float4*>(static_cast<float*>(out_) + (int64_t)m * C + col) = t;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&lo);
+            o.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out_) + (int64_t)m * C + col) = o;
+        }
+    }
+}
+
+template <int K, int NPAD>
+cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, const SplitSchedule& sc, float* partial,
+                      float* fix, int* status, cudaStream_t stream) {
+    const int smem = StLayout<NPAD>::kAlloc;
+    cudaError_t e = cudaFuncSetAttribute(scatter_tc_kernel<K, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(scatter_tc_kernel<K, NPAD>, dim3((unsigned)sc.G), dim3(kStThreads), (size_t)smem, stream, x, M,
+                      p.codes, p.scales, p.lut, (int)p.cols, p.interleave, sc, partial, fix, status);
+}
+
+template <int K>
+cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, const SplitSchedule& sc, float* partial,
+                     float* fix, int* status, cudaStream_t stream) {
+    if (M <= 16) return launch_kn<K, 16>(p, x, M, sc, partial, fix, status, stream);
+    return launch_kn<K, 32>(p, x, M, sc, partial, fix, status, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_scatter_tc(const Packed& p, const uint16_t* x, int M, int splits, float* partial,
+                              float* fix, void* out, bool out_f32, int* status, int sm_count,
+                              cudaStream_t stream) {
+    const int64_t C = p.cols;
+    SplitSchedule sc = SplitSchedule::make(p.rows, splits, C, 1);
+    int64_t G = sm_count < kScatterTcMaxCtas ? sm_count : kScatterTcMaxCtas;
+    if (G > sc.T) G = sc.T;
+    if (G < 1) G = 1;
+    sc.G = (int)G;
+    cudaError_t e;
+    switch (p.k) {
+        case 2: e = launch_k<2>(p, x, M, sc, partial, fix, status, stream); break;
+        case 3: e = launch_k<3>(p, x, M, sc, partial, fix, status, stream); break;
+        case 4: e = launch_k<4>(p, x, M, sc, partial, fix, status, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = out_f32 ? launch_pdl(tc_split_reduce_kernel<true>, dim3((unsigned)(C / 32), (unsigned)M), dim3(256), 0,
+                             stream, partial, static_cast<const float*>(fix), sc, M, (int)C, out)
+                : launch_pdl(tc_split_reduce_kernel<false>, dim3((unsigned)(C / 32), (unsigned)M), dim3(256), 0,
+                             stream, partial, static_cast<const float*>(fix), sc, M, (int)C, out);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace tcq

@@ -1,5 +1,5 @@
-// Thin inline-PTX wrappers for the sm_100-family features the prefill kernel
-// uses: mbarriers, tensor memory (tcgen05.alloc/ld/st), the tcgen05 MMA and
+// Thin inline-PTX wrappers for the sm_100-family features the tensor-core
+// kernels use: mbarriers, tensor memory (tcgen05.alloc/ld/st), the tcgen05 MMA and
 // the async-proxy fence.  Every wait is bounded by a wall-clock deadline.
 #pragma once
 
@@ -117,6 +117,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t sbo) {
     d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
     return d;
 }
+// Shared-memory matrix descriptor, MN-major (M or N contiguous), 128-byte
+// swizzle: an atom is 8 K-rows of 128 bytes (64 bf16 along M/N), 1024
+// bytes; `lbo` is the byte distance between atoms along M/N, `sbo` between
+// atoms along K.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;      // leading byte offset: next atom along M/N
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;      // stride byte offset: next 8 rows of K
+    d |= (uint64_t)1 << 46;                            // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
+    return d;
+}
 // Instruction descriptor of kind::f16: bf16 A and B, f32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
     return (1u << 4)                       // D format f32
@@ -132,6 +145,31 @@ __device__ __forceinline__ void mma_ts(uint32_t d_taddr, uint32_t a_taddr, uint6
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_taddr), "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// The same with A MN-major (bit 15, "transpose A").
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int m, int n) {
+    return idesc_bf16_f32(m, n) | (1u << 15);
+}
+// D(tmem) (+)= A(smem) * B(smem), issued by one thread.
+__device__ __forceinline__ void mma_ss(uint32_t d_taddr, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_taddr), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 32 consecutive 32-bit columns of this thread's lane (warp-wide, 32x32b shape)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr) : "memory");
 }
 // Arrive on the mbarrier once all previously issued MMAs of this thread finish.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
