@@ -20,13 +20,14 @@
 //     64q + 8g .. +7 of the block, region r holding columns 64q + 8g + 2r
 //     (lane 32q+g) and 64q + 8g + 2r + 1 (lane 32q+g+8).  The rows of D past
 //     lane 16 of a quarter are never read;
-//   - B (activations x[m][r0 .. r0+63]) is K-major with the 128-byte swizzle,
-//     copied by one loader warp with cp.async (zero rows past M and past the
-//     split) into a ring of 4 stages;
-//   - the code words of a stage (its rows of one block) are copied by a code
-//     loader warp with cp.async into a ring of 3 tiles of 128-byte rows, the
-//     16-byte chunks of row r rotated by 2 * ((r / 4) % 4) so that the four
-//     rows a warp reads at once sit in four different bank groups;
+//   - B (activations x[m][r0 .. r0+63]) is K-major with the 128-byte swizzle;
+//   - a loader warp fills a ring of 4 slots, each the bundle of one stage:
+//     its code words (64 rows of one block, 128 bytes each), its 64 row
+//     scales and B, all by TMA tensor copies on one mbarrier, up to 4 stages
+//     ahead.  The copies bypass the load/store pipe that the codebook
+//     gathers keep busy (per-thread cp.async copies there took microseconds
+//     to land).  Rows whose first index is not a multiple of 8 fall back to
+//     plain copies for the scales and B;
 //   - D (fp32) lives in tensor memory, two buffers of 4 regions x N columns,
 //     so the epilogue of one item overlaps the MMAs of the next.
 // A stage is up to 64 rows (4 K steps) of one item (one split, one block of
@@ -37,10 +38,16 @@
 //
 // Warps: 16 decoders (warp w: lane quarter w % 4, K step w / 4 of the stage;
 // a thread decodes 8 windows of each of its 4 rows from 3 words of the code
-// tile), 4 epilogue warps (lane quarters 0..3), 1 MMA warp, 1 activation
-// loader, 1 code loader.  Every mbarrier wait is bounded (1 s); a wait that
+// tile), 4 epilogue warps (lane quarters 0..3), 1 MMA warp, 1 loader.
+// The barriers are few on purpose: each wait costs a few hundred cycles even
+// when the phase is already complete, and the MMA warp's chain of waits per
+// stage set the pace of an earlier version.  Every mbarrier wait is bounded (1 s); a wait that
 // gives up sets the CTA's abort flag and the device status word, and the
 // kernel returns without further output.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "splitk_schedule.cuh"
@@ -52,27 +59,36 @@ namespace {
 constexpr int kStDecWarps = 16;                 // warps 16..19: epilogue, lane quarters 0..3
 constexpr int kStMmaWarp = 20;
 constexpr int kStActWarp = 21;
-constexpr int kStCodeWarp = 22;
-constexpr int kStThreads = 23 * 32;
+constexpr int kStThreads = 22 * 32;
 constexpr int kStRows = 64;                     // rows (K) of a stage: 4 MMA steps of 16
 constexpr int kStSteps = kStRows / 16;
-constexpr int kStStages = 2;                    // stages of decoded weights (A, tensor memory)
-constexpr int kStBStages = 4;                   // stages of activations (B)
-constexpr int kStCStages = 3;                   // stages of code tiles
+constexpr int kStStages = 3;                    // stages of decoded weights (A, tensor memory)
+constexpr int kStCStages = 4;                   // stages of code tiles
 constexpr int kStPitch = 128;                   // bytes per row of a code tile
 constexpr int kStCBytes = kStRows * kStPitch;   // one code tile (8 KB)
+// Per code slot, written by the loader with the tile: the stage's 64 row
+// scales (bf16) and a descriptor: take, valid rows, whether another stage
+// follows.
+constexpr int kStSclBytes = kStRows * 2;
 constexpr uint32_t kStTmemCols = 512;
-constexpr uint32_t kStACol = 256;               // A stages at [256, 512): 4 regions x 32 columns each
+// A stages at [128, 512): 4 regions x 32 columns each; D buffers at [0, 128):
+// two of 4 regions x 16 columns, or one of 4 x 32
+constexpr uint32_t kStACol = kStTmemCols - kStStages * 128;
+__host__ __device__ constexpr int st_dbufs(int npad) { return 4 * npad * 2 <= (int)kStACol ? 2 : 1; }
 constexpr uint64_t kStWaitNs = 1000000000ull;
 
 template <int NPAD>
 struct StLayout {
     static constexpr int kB = NPAD * 128;       // activations of one stage: NPAD rows x 64 K
-    static constexpr int kBOff = 0;
-    static constexpr int kCOff = kBOff + kStBStages * kB;
-    static constexpr int kLutOff = kCOff + kStCStages * kStCBytes;
+    static constexpr int kCOff = 0;             // code tiles: 1024-byte aligned for the swizzled TMA
+    static constexpr int kBOff = kCOff + kStCStages * kStCBytes;
+    // per code slot: the stage's 64 row scales (TMA destination: 128-byte
+    // aligned, here 1024) and its 16-byte descriptor
+    static constexpr int kSclOff = kBOff + kStCStages * kB;
+    static constexpr int kInfoOff = kSclOff + kStCStages * kStSclBytes;
+    static constexpr int kLutOff = (kInfoOff + kStCStages * 16 + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
-    // 32 mbarriers, the tensor-memory address and the abort flag
+    // 34 mbarriers, the tensor-memory address and the abort flag
     static constexpr int kBarBytes = 320;
     static constexpr int kBytes = kBarOff + kBarBytes;
     static constexpr int kAlloc = kBytes + 1024;    // slack for 1024-byte alignment
@@ -134,11 +150,11 @@ __device__ __forceinline__ bool next_stage(const SplitSchedule& sc, Cursor& c, S
     return true;
 }
 
-// Byte offset of word w of row r in a code tile (16-byte chunks rotated by
-// 2 * ((r / 4) % 4) within the 128-byte row).
+// Byte offset of word w of row r in a code tile written by the TMA with the
+// 128-byte swizzle (tile 1024-byte aligned): the 16-byte chunk index of the
+// row is XOR-ed with r mod 8.
 __device__ __forceinline__ uint32_t ctile_off(int r, int w) {
-    return (uint32_t)r * kStPitch + ((((uint32_t)w >> 2) + 2u * (((uint32_t)r >> 2) & 3u)) & 7u) * 16u +
-           ((uint32_t)w & 3u) * 4u;
+    return (uint32_t)r * kStPitch + ((((uint32_t)w >> 2) ^ ((uint32_t)r & 7u)) << 4) + ((uint32_t)w & 3u) * 4u;
 }
 
 // tcgen05.st of 4 registers per thread in the 16x256b shape: thread (g, c)
@@ -153,8 +169,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
 scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const float* __restrict__ lut,
                   int C, int interleave, SplitSchedule sc, float* __restrict__ partial,
-                  float* __restrict__ fix, int* __restrict__ status) {
+                  float* __restrict__ fix, int* __restrict__ status, const __grid_constant__ CUtensorMap tmap,
+                  const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap, int tma_x) {
     using Lay = StLayout<NPAD>;
+    constexpr int kDBuf = st_dbufs(NPAD);
+    static_assert(kDBuf * 4 * NPAD <= (int)kStACol, "D buffers overlap the A stages");
     extern __shared__ uint8_t smem_raw[];
     // nothing is read, written or allocated before the previous kernel of
     // the stream has completed
@@ -162,38 +181,40 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
     pdl_release();
     uint8_t* base = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
     float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
-    // afull[stage][step]: the 4 warps of one 16-row step wrote their part of
-    // A, so that step's 4 MMAs can go
+    // Per stage of A (tensor memory): afull -- all decoders wrote it;
+    // aempty -- the MMAs that read it are done.  Per slot (codes, scales and
+    // activations of one stage, one TMA bundle): cfull -- landed; sempty --
+    // the stage's MMAs are done, which is after every decoder read the slot.
     uint64_t* afull = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);
-    uint64_t* aempty = afull + kStStages * kStSteps;                       // MMA done with A
-    uint64_t* bfull = aempty + kStStages;                                  // loader wrote B
-    uint64_t* bempty = bfull + kStBStages;                                 // MMA done with B
-    uint64_t* cfull = bempty + kStBStages;                                 // code tile landed
-    uint64_t* cempty = cfull + kStCStages;                                 // code tile read
-    uint64_t* dfull = cempty + kStCStages;                                 // an item's D complete
+    uint64_t* aempty = afull + kStStages;
+    uint64_t* cfull = aempty + kStStages;
+    uint64_t* sempty = cfull + kStCStages;
+    uint64_t* dfull = sempty + kStCStages;                                 // an item's D complete
     uint64_t* dempty = dfull + 2;                                          // epilogue done with D
     uint64_t* done = dempty + 2;                                           // every MMA complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    static_assert((kStStages * kStSteps + kStStages + 2 * kStBStages + 2 * kStCStages + 5) * 8 + 8 <= Lay::kBarBytes,
-                  "barrier area too small");
+    static_assert((2 * kStStages + 2 * kStCStages + 5) * 8 + 8 <= Lay::kBarBytes, "barrier area too small");
+    // every TMA destination: tiles 1024-byte aligned (128-byte swizzle), the
+    // scales 128-byte aligned
+    static_assert(Lay::kCOff % 1024 == 0 && kStCBytes % 1024 == 0 && Lay::kBOff % 1024 == 0 && Lay::kB % 1024 == 0,
+                  "swizzled TMA destinations must be 1024-byte aligned");
+    static_assert(Lay::kSclOff % 128 == 0 && kStSclBytes % 128 == 0, "TMA destinations must be 128-byte aligned");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     stage_lut_rep8(lut_s, lut);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStStages * kStSteps; ++i) tc::mbar_init(&afull[i], 4 * 32);
-        for (int i = 0; i < kStStages; ++i) tc::mbar_init(&aempty[i], 1);
-        for (int i = 0; i < kStBStages; ++i) {
-            tc::mbar_init(&bfull[i], 32);
-            tc::mbar_init(&bempty[i], 1);
+        for (int i = 0; i < kStStages; ++i) {
+            tc::mbar_init(&afull[i], kStDecWarps * 32);
+            tc::mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < kStCStages; ++i) {
-            tc::mbar_init(&cfull[i], 32);
-            tc::mbar_init(&cempty[i], kStDecWarps * 32);
+            tc::mbar_init(&cfull[i], 1);
+            tc::mbar_init(&sempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&dfull[i], 1);
-            tc::mbar_init(&dempty[i], 4 * 32);
+            tc::mbar_init(&dempty[i], 4);
         }
         tc::mbar_init(done, 1);
         *abort_flag = 0;
@@ -230,48 +251,76 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
         const int w2i = wi + 2 < wpb ? wi + 2 : wi + 2 - wpb;
         // this thread's rows of the stage: 16 ks + 4c + i, i = 0..3
         const int row0 = 16 * ks + 4 * c;
-        uint32_t woff[3];
-        woff[0] = ctile_off(row0, wi);
-        woff[1] = ctile_off(row0, w1i);
-        woff[2] = ctile_off(row0, w2i);
+        const int widx[3] = {wi, w1i, w2i};
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        Cursor cur;
-        cursor_init(sc, cur, xb, xe);
-        Stage st;
-        for (int j = 0; next_stage(sc, cur, st); ++j) {
-            const int as = j % kStStages, cs = j % kStCStages;
-            const bool active = ks < st.take;
-            uint32_t pk[16];
-            if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[cs], (j / kStCStages) & 1, abort_flag, kStWaitNs)))
-                break;
-            if (active) {
-                // words and scales of the 4 rows, then the tile is released
-                uint32_t wv[4][3];
-                float sv[4];
-                const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
+        const uint32_t info_base = s_base + Lay::kInfoOff;
+        const uint32_t scl_base = s_base + Lay::kSclOff;
+        // What a decoder thread takes from code slot cs once it has landed:
+        // the stage's take / valid / more, this thread's 4 scales and the 3
+        // words of each of its 4 rows.  The slot is released right after.
+        struct Held { int take, valid, more; float sv[4]; uint32_t wv[4][3]; };
+        auto take_slot = [&](int cs, Held& h) {
+            const uint32_t info = info_base + (uint32_t)cs * 16u;
+            uint32_t d0, d1, d2, d3, s01, s23;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3) : "r"(info));
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(s01), "=r"(s23)
+                         : "r"(scl_base + (uint32_t)cs * kStSclBytes + 2u * (uint32_t)row0));
+            (void)d3;
+            h.take = (int)d0;
+            h.valid = (int)d1;
+            h.more = (int)d2;
+            h.sv[0] = bf16_bits_to_float(s01 & 0xffffu);
+            h.sv[1] = bf16_bits_to_float(s01 >> 16);
+            h.sv[2] = bf16_bits_to_float(s23 & 0xffffu);
+            h.sv[3] = bf16_bits_to_float(s23 >> 16);
+            const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) {
                 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool in = row0 + i < st.valid;
-                    #pragma unroll
-                    for (int t = 0; t < 3; ++t) {
-                        uint32_t v;
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + woff[t] + (uint32_t)i * kStPitch));
-                        wv[i][t] = in ? v : 0u;
-                    }
-                    sv[i] = in ? bf16_bits_to_float(__ldg(scales + st.r_begin + row0 + i)) : 0.f;
+                for (int t = 0; t < 3; ++t) {
+                    uint32_t v;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + ctile_off(row0 + i, widx[t])));
+                    h.wv[i][t] = v;
                 }
-                tc::mbar_arrive(&cempty[cs]);
+            }
+        };
+        Held h0, h1;
+        bool have = xb < xe;
+        if (have) {
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[0], 0, abort_flag, kStWaitNs))) have = false;
+            else take_slot(0, h0);
+        }
+        for (int j = 0; have; ++j) {
+            const int as = j % kStStages;
+            const bool more = h0.more != 0;
+            // the next stage's slot, read while this stage is decoded
+            if (more) {
+                const int cn = (j + 1) % kStCStages;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[cn], ((j + 1) / kStCStages) & 1, abort_flag, kStWaitNs)))
+                    break;
+                take_slot(cn, h1);
+            }
+            const bool active = ks < h0.take;
+            uint32_t pk[16];
+            if (active) {
+                // rows past the split enter the MMA as zeros
+                #pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (row0 + i >= h0.valid) {
+                        h0.sv[i] = 0.f;
+                        h0.wv[i][0] = h0.wv[i][1] = h0.wv[i][2] = 0u;
+                    }
                 // bits [S, S + 64) of each row: the window of column t0+e at bit (7-e) k
                 uint32_t ww[4][2];
                 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    ww[i][0] = __funnelshift_r(wv[i][0], wv[i][1], off);
-                    ww[i][1] = __funnelshift_r(wv[i][1], wv[i][2], off);
+                    ww[i][0] = __funnelshift_r(h0.wv[i][0], h0.wv[i][1], off);
+                    ww[i][1] = __funnelshift_r(h0.wv[i][1], h0.wv[i][2], off);
                 }
                 // region r: lane g <- column t0+2r, lane g+8 <- column t0+2r+1;
                 // registers (rows 4c, 4c+1) and (rows 4c+2, 4c+3) of each
                 auto wgt = [&](int i, int e) {
-                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), sv[i]);
+                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), h0.sv[i]);
                 };
                 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -280,8 +329,6 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                     pk[4 * r + 2] = pack_bf16x2(wgt(0, 2 * r + 1), wgt(1, 2 * r + 1));
                     pk[4 * r + 3] = pack_bf16x2(wgt(2, 2 * r + 1), wgt(3, 2 * r + 1));
                 }
-            } else {
-                tc::mbar_arrive(&cempty[cs]);
             }
             // the warp leaves together: a wait that gave up in one lane ends the loop in all
             if (j >= kStStages &&
@@ -296,75 +343,96 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                 tc::tmem_wait_st();
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&afull[as * kStSteps + ks]);
+            tc::mbar_arrive(&afull[as]);
+            h0 = h1;
+            have = more;
         }
-    } else if (warp == kStCodeWarp) {
-        // ------------------------------------------------------------ code loader
-        // The stage's rows of block b in 16-byte cp.async chunks (a warp
-        // instruction covers 4 to 2 rows), rotated within the 128-byte tile
-        // rows; each lane's copies arrive on cfull[cs] when they land.
-        const int64_t rs = block_row_stride(C / kBT, wpb, interleave);
-        constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
+    } else if (warp == kStActWarp) {
+        // ------------------------------------------------------------ loader
+        // One bundle per slot: the stage's code tile (rows r_begin .. +63 of
+        // block b, 32 words from the block's first; rows past the matrix and
+        // words past its row arrive as zeros), its 64 row scales, and the
+        // activation tile x[0 .. NPAD)[r_begin .. +64) (K-major, 128-byte
+        // swizzle; rows past M and past the matrix as zeros, rows past the
+        // split meet zero weights).  Slot j % 4 was last used by stage j - 4.
+        const uint64_t tmap_ptr = reinterpret_cast<uint64_t>(&tmap);
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(tmap_ptr) : "memory");
         Cursor cur;
         cursor_init(sc, cur, xb, xe);
         Stage st;
         for (int j = 0; next_stage(sc, cur, st); ++j) {
             const int cs = j % kStCStages;
-            if (j >= kStCStages &&
-                !__all_sync(0xffffffffu, tc::mbar_wait(&cempty[cs], ((j / kStCStages) - 1) & 1, abort_flag, kStWaitNs)))
-                break;
-            const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
-            const uint32_t* src0 = codes + block_col_base(st.b, R, wpb, interleave) + st.r_begin * rs;
-            const int nchunks = st.valid * cpr;
-            for (int ch = lane; ch < nchunks; ch += 32) {
-                const int r = ch / cpr, part = ch - (ch / cpr) * cpr;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             :: "r"(tile + ctile_off(r, 4 * part)), "l"(src0 + (int64_t)r * rs + 4 * part)
-                             : "memory");
-            }
-            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
-                         :: "r"(tc::smem_addr(&cfull[cs])) : "memory");
-        }
-    } else if (warp == kStActWarp) {
-        // ------------------------------------------------------------ activation loader
-        Cursor cur;
-        cursor_init(sc, cur, xb, xe);
-        Stage st;
-        for (int j = 0; next_stage(sc, cur, st); ++j) {
-            const int bs_i = j % kStBStages;
-            if (j >= kStBStages &&
-                !__all_sync(0xffffffffu, tc::mbar_wait(&bempty[bs_i], ((j / kStBStages) - 1) & 1, abort_flag, kStWaitNs)))
-                break;
-            const uint32_t bs = b_base + (uint32_t)bs_i * Lay::kB;
-            #pragma unroll 1
-            for (int idx = lane; idx < NPAD * 8; idx += 32) {
-                const int n = idx >> 3, c8 = idx & 7;
-                const uint32_t dst = bs + (uint32_t)n * 128u + ((uint32_t)(c8 ^ (n & 7)) << 4);
-                int cnt = st.valid - 8 * c8;
-                cnt = cnt < 0 ? 0 : cnt > 8 ? 8 : cnt;
-                const int64_t e = (int64_t)n * R + st.r_begin + 8 * c8;
-                if (n < M && cnt == 8 && (e & 7) == 0) {
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(x + e) : "memory");
-                } else if (n < M && cnt > 0) {
-                    uint32_t v[4];
-                    #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t lo = 2 * q < cnt ? (uint32_t)__ldg(x + e + 2 * q) : 0u;
-                        const uint32_t hi = 2 * q + 1 < cnt ? (uint32_t)__ldg(x + e + 2 * q + 1) : 0u;
-                        v[q] = lo | (hi << 16);
+            if (j >= kStCStages && !tc::warp_wait(&sempty[cs], ((j / kStCStages) - 1) & 1, abort_flag, kStWaitNs)) break;
+            const uint32_t bar = tc::smem_addr(&cfull[cs]);
+            const uint32_t bs = b_base + (uint32_t)cs * Lay::kB;
+            if (!tma_x) {
+                // scales and activations with plain copies (rows that do not
+                // start on a 16-byte boundary), complete before the arrival
+                const int r2 = 2 * lane;
+                const uint32_t lo = r2 < st.valid ? (uint32_t)__ldg(scales + st.r_begin + r2) : 0u;
+                const uint32_t hi = r2 + 1 < st.valid ? (uint32_t)__ldg(scales + st.r_begin + r2 + 1) : 0u;
+                reinterpret_cast<uint32_t*>(base + Lay::kSclOff + cs * kStSclBytes)[lane] = lo | (hi << 16);
+                #pragma unroll 1
+                for (int idx = lane; idx < NPAD * 8; idx += 32) {
+                    const int n = idx >> 3, c8 = idx & 7;
+                    const uint32_t dst = bs + (uint32_t)n * 128u + ((uint32_t)(c8 ^ (n & 7)) << 4);
+                    int cnt = st.valid - 8 * c8;
+                    cnt = cnt < 0 ? 0 : cnt > 8 ? 8 : cnt;
+                    const int64_t e = (int64_t)n * R + st.r_begin + 8 * c8;
+                    uint32_t v[4] = {0u, 0u, 0u, 0u};
+                    if (n < M && cnt > 0) {
+                        #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t l16 = 2 * q < cnt ? (uint32_t)__ldg(x + e + 2 * q) : 0u;
+                            const uint32_t h16 = 2 * q + 1 < cnt ? (uint32_t)__ldg(x + e + 2 * q + 1) : 0u;
+                            v[q] = l16 | (h16 << 16);
+                        }
                     }
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                  :: "r"(dst), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
+                }
+                tc::fence_proxy_async_smem();
+            }
+            if (lane == 0) {
+                int* d = reinterpret_cast<int*>(base + Lay::kInfoOff + cs * 16);
+                d[0] = st.take;
+                d[1] = st.valid;
+                d[2] = cur.x < cur.xe ? 1 : 0;
+                d[3] = 0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t dst = c_base + (uint32_t)cs * kStCBytes;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                             :: "r"(bar), "r"(kStCBytes + (tma_x ? kStSclBytes + Lay::kB : 0)) : "memory");
+                if (tma_x) {
+                    asm volatile("cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2}], [%3];"
+                                 :: "r"(s_base + (uint32_t)(Lay::kSclOff + cs * kStSclBytes)),
+                                    "l"(reinterpret_cast<uint64_t>(&smap)), "r"((int)st.r_begin), "r"(bar) : "memory");
+                    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3}], [%4];"
+                                 :: "r"(bs), "l"(reinterpret_cast<uint64_t>(&xmap)), "r"((int)st.r_begin), "r"(0),
+                                    "r"(bar) : "memory");
+                }
+                if (interleave == 2) {
+                    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                                 :: "r"(dst), "l"(tmap_ptr), "r"((st.b & 1) * wpb), "r"((int)st.r_begin), "r"(st.b >> 1),
+                                    "r"(bar) : "memory");
                 } else {
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" :: "r"(dst), "l"(x) : "memory");
+                    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3}], [%4];"
+                                 :: "r"(dst), "l"(tmap_ptr), "r"(st.b * wpb), "r"((int)st.r_begin), "r"(bar) : "memory");
                 }
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&bfull[bs_i]);
+            __syncwarp();
         }
     } else if (warp == kStMmaWarp) {
         // ------------------------------------------------------------ MMA issue
+        // One wait per stage: the decoders arrive on afull after they took
+        // the stage's slot, so the slot's activations have landed too.  One
+        // commit frees the A stage and one the slot.
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, NPAD);
             Cursor cur;
@@ -374,31 +442,25 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             for (int j = 0; next_stage(sc, cur, st); ++j) {
                 if (st.first) {
                     ++ic;
-                    if (ic >= 2 && !tc::mbar_wait(&dempty[ic & 1], ((ic >> 1) - 1) & 1, abort_flag, kStWaitNs))
+                    if (ic >= kDBuf &&
+                        !tc::mbar_wait(&dempty[ic % kDBuf], ((ic / kDBuf) - 1) & 1, abort_flag, kStWaitNs))
                         break;
                 }
-                const int as = j % kStStages, bs_i = j % kStBStages;
-                if (!tc::mbar_wait(&bfull[bs_i], (j / kStBStages) & 1, abort_flag, kStWaitNs)) break;
-                const uint32_t d = tmem + (uint32_t)(ic & 1) * (4 * NPAD);
-                const uint32_t bsa = b_base + (uint32_t)bs_i * Lay::kB;
-                // each 16-row step as soon as its four warps are done
-                bool ok = true;
+                const int as = j % kStStages, cs = j % kStCStages;
+                if (!tc::mbar_wait(&afull[as], (j / kStStages) & 1, abort_flag, kStWaitNs)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(ic % kDBuf) * (4 * NPAD);
+                const uint32_t bsa = b_base + (uint32_t)cs * Lay::kB;
                 for (int kk = 0; kk < st.take; ++kk) {
-                    if (!tc::mbar_wait(&afull[as * kStSteps + kk], (j / kStStages) & 1, abort_flag, kStWaitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
                     const uint64_t bd = tc::sdesc_sw128(bsa + (uint32_t)kk * 32u, 1024u);
                     #pragma unroll
                     for (int r = 0; r < 4; ++r)
                         tc::mma_ts(d + (uint32_t)r * NPAD, tmem + kStACol + (uint32_t)(as * 128 + r * 32 + kk * 8), bd,
                                    idesc, (st.first && kk == 0) ? 0u : 1u);
                 }
-                if (!ok) break;
                 tc::mma_commit(&aempty[as]);
-                tc::mma_commit(&bempty[bs_i]);
-                if (st.last) tc::mma_commit(&dfull[ic & 1]);
+                tc::mma_commit(&sempty[cs]);
+                if (st.last) tc::mma_commit(&dfull[ic % kDBuf]);
             }
             tc::mma_commit(done);
         }
@@ -418,8 +480,8 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                 from_zero = st.k == 0;
             }
             if (!st.last) continue;
-            const int d = ic & 1;
-            if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[d], (ic >> 1) & 1, abort_flag, kStWaitNs))) break;
+            const int d = ic % kDBuf;
+            if (!tc::warp_wait(&dfull[d], (ic / kDBuf) & 1, abort_flag, kStWaitNs)) break;
             tc::tc_fence_after();
             // the CTA that holds the item's first step writes the partial
             // itself; a CTA that starts inside an item (only ever its first
@@ -446,7 +508,7 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                 }
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&dempty[d]);
+            tc::warp_arrive(&dempty[d]);
         }
     }
 
@@ -524,21 +586,108 @@ tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fi
     }
 }
 
+// cuTensorMapEncodeTiled, found once through the runtime (no link-time
+// dependence on the driver library).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, []() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// The codes as a tensor of uint32 words: interleave 0 is [rows][words of a
+// row]; interleave 2 is [block pairs][rows][2 * wpb].  The box is 32 words
+// (128 bytes, one swizzle row) by 64 rows.
+cudaError_t code_tensor_map(const Packed& p, CUtensorMap* map) {
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const int wpb = kBT * p.k / 32;
+    const cuuint64_t nb = (cuuint64_t)(p.cols / kBT);
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3] = {32, (cuuint32_t)kStRows, 1}, estr[3] = {1, 1, 1};
+    cuuint32_t rank;
+    if (p.interleave == 2) {
+        rank = 3;
+        dims[0] = 2 * (cuuint64_t)wpb;
+        dims[1] = (cuuint64_t)p.rows;
+        dims[2] = nb / 2;
+        strides[0] = dims[0] * 4;
+        strides[1] = strides[0] * dims[1];
+    } else {
+        rank = 2;
+        dims[0] = nb * (cuuint64_t)wpb;
+        dims[1] = (cuuint64_t)p.rows;
+        strides[0] = dims[0] * 4;
+    }
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<uint32_t*>(p.codes), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The activations x [M][R] (bf16) with a box of 64 input rows by npad
+// activation rows and the 128-byte swizzle, which is the MMA's K-major B
+// layout; and the scales [R] (bf16) with a box of 64.
+cudaError_t act_tensor_maps(const Packed& p, const uint16_t* x, int M, int npad, CUtensorMap* xmap,
+                            CUtensorMap* smap) {
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t xd[2] = {(cuuint64_t)p.rows, (cuuint64_t)M};
+    const cuuint64_t xs[1] = {(cuuint64_t)p.rows * 2};
+    const cuuint32_t xb[2] = {(cuuint32_t)kStRows, (cuuint32_t)npad};
+    CUresult r = enc(xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(x), xd, xs, xb, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t sd[1] = {(cuuint64_t)p.rows};
+    const cuuint32_t sb[1] = {(cuuint32_t)kStRows};
+    const cuuint64_t ss[1] = {(cuuint64_t)p.rows * 2};   // not read for a rank-1 tensor
+    r = enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<uint16_t*>(p.scales), sd, ss, sb, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int K, int NPAD>
 cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, const SplitSchedule& sc, float* partial,
-                      float* fix, int* status, cudaStream_t stream) {
+                      float* fix, int* status, const CUtensorMap& map, cudaStream_t stream) {
     const int smem = StLayout<NPAD>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(scatter_tc_kernel<K, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // TMA for the activations and scales when every stage's first row is a
+    // multiple of 8 (16 bytes of bf16) and x, scales and rows allow it
+    const bool tma_x = p.rows % 8 == 0 && sc.rp % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0;
+    alignas(64) CUtensorMap xmap, smap;
+    if (tma_x) {
+        e = act_tensor_maps(p, x, M, NPAD, &xmap, &smap);
+        if (e != cudaSuccess) return e;
+    } else {
+        xmap = map;                    // unused
+        smap = map;
+    }
     return launch_pdl(scatter_tc_kernel<K, NPAD>, dim3((unsigned)sc.G), dim3(kStThreads), (size_t)smem, stream, x, M,
-                      p.codes, p.scales, p.lut, (int)p.cols, p.interleave, sc, partial, fix, status);
+                      p.codes, p.scales, p.lut, (int)p.cols, p.interleave, sc, partial, fix, status, map, xmap,
+                      smap, tma_x ? 1 : 0);
 }
 
 template <int K>
 cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, const SplitSchedule& sc, float* partial,
-                     float* fix, int* status, cudaStream_t stream) {
-    if (M <= 16) return launch_kn<K, 16>(p, x, M, sc, partial, fix, status, stream);
-    return launch_kn<K, 32>(p, x, M, sc, partial, fix, status, stream);
+                     float* fix, int* status, const CUtensorMap& map, cudaStream_t stream) {
+    if (M <= 16) return launch_kn<K, 16>(p, x, M, sc, partial, fix, status, map, stream);
+    return launch_kn<K, 32>(p, x, M, sc, partial, fix, status, map, stream);
 }
 
 }  // namespace
@@ -552,11 +701,13 @@ cudaError_t launch_scatter_tc(const Packed& p, const uint16_t* x, int M, int spl
     if (G > sc.T) G = sc.T;
     if (G < 1) G = 1;
     sc.G = (int)G;
-    cudaError_t e;
+    alignas(64) CUtensorMap map;
+    cudaError_t e = code_tensor_map(p, &map);
+    if (e != cudaSuccess) return e;
     switch (p.k) {
-        case 2: e = launch_k<2>(p, x, M, sc, partial, fix, status, stream); break;
-        case 3: e = launch_k<3>(p, x, M, sc, partial, fix, status, stream); break;
-        case 4: e = launch_k<4>(p, x, M, sc, partial, fix, status, stream); break;
+        case 2: e = launch_k<2>(p, x, M, sc, partial, fix, status, map, stream); break;
+        case 3: e = launch_k<3>(p, x, M, sc, partial, fix, status, map, stream); break;
+        case 4: e = launch_k<4>(p, x, M, sc, partial, fix, status, map, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

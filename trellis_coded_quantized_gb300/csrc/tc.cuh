@@ -37,24 +37,49 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
+// Potentially blocking test: the thread may be suspended by the hardware
+// until the phase completes (or a system-dependent time runs out), so a
+// waiting warp does not keep issuing shared-memory operations.
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall-clock time, or as soon as *abort is set by another
 // thread; returns false in both cases (and sets *abort on a timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;       // non-blocking fast path
+    if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort = 1;
-                return false;
-            }
-            __nanosleep(64);
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
         }
     }
+}
+
+// Warp-level forms: lane 0 alone waits or arrives, the others follow through
+// __syncwarp (which orders the warp's memory accesses around it), so a
+// barrier sees one operation per warp instead of 32.  All 32 lanes must call
+// them.  warp_wait returns the same result in every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // ---------------------------------------------------------------- proxies
