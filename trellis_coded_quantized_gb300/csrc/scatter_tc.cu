@@ -38,10 +38,11 @@
 //
 // Warps: 16 decoders (warp w: lane quarter w % 4, K step w / 4 of the stage;
 // a thread decodes 8 windows of each of its 4 rows from 3 words of the code
-// tile), 4 epilogue warps (lane quarters 0..3), 1 MMA warp, 1 loader.
+// tile), 4 epilogue warps (lane quarters 0..3), 4 MMA warps (region r each),
+// 1 loader.  One thread issues an MMA only every 60-100 cycles whatever its
+// shape, so the 16 MMAs of a stage go out from four threads at once.
 // The barriers are few on purpose: each wait costs a few hundred cycles even
-// when the phase is already complete, and the MMA warp's chain of waits per
-// stage set the pace of an earlier version.  Every mbarrier wait is bounded (1 s); a wait that
+// when the phase is already complete.  Every mbarrier wait is bounded (1 s); a wait that
 // gives up sets the CTA's abort flag and the device status word, and the
 // kernel returns without further output.
 #include <cuda.h>
@@ -57,9 +58,9 @@ namespace tcq {
 namespace {
 
 constexpr int kStDecWarps = 16;                 // warps 16..19: epilogue, lane quarters 0..3
-constexpr int kStMmaWarp = 20;
-constexpr int kStActWarp = 21;
-constexpr int kStThreads = 22 * 32;
+constexpr int kStMmaWarp = 20;                  // warps 20..23: MMA issue, one region each
+constexpr int kStActWarp = 24;
+constexpr int kStThreads = 25 * 32;
 constexpr int kStRows = 64;                     // rows (K) of a stage: 4 MMA steps of 16
 constexpr int kStSteps = kStRows / 16;
 constexpr int kStStages = 3;                    // stages of decoded weights (A, tensor memory)
@@ -206,17 +207,17 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStStages; ++i) {
             tc::mbar_init(&afull[i], kStDecWarps * 32);
-            tc::mbar_init(&aempty[i], 1);
+            tc::mbar_init(&aempty[i], 4);
         }
         for (int i = 0; i < kStCStages; ++i) {
             tc::mbar_init(&cfull[i], 1);
-            tc::mbar_init(&sempty[i], 1);
+            tc::mbar_init(&sempty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&dfull[i], 1);
+            tc::mbar_init(&dfull[i], 4);
             tc::mbar_init(&dempty[i], 4);
         }
-        tc::mbar_init(done, 1);
+        tc::mbar_init(done, 4);
         *abort_flag = 0;
         tc::mbar_init_fence();
     }
@@ -249,16 +250,24 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
         const uint32_t off = (uint32_t)(S & 31);
         const int w1i = wi + 1 < wpb ? wi + 1 : wi + 1 - wpb;
         const int w2i = wi + 2 < wpb ? wi + 2 : wi + 2 - wpb;
-        // this thread's rows of the stage: 16 ks + 4c + i, i = 0..3
+        // this thread's rows of the stage: 16 ks + 4c + i, i = 0..3.  Held
+        // words slot i carries row 4c + (i ^ sw): threads c = 2, 3 load their
+        // rows in the order 2, 3, 0, 1, so that in every word load the four c
+        // of a warp read tile rows whose 128-byte swizzle phases (row mod 8)
+        // differ by 2, 4 or 6 and no two of them meet in a bank (rows 8
+        // apart, the same phase, would).  The decode puts the rows back in
+        // order.
         const int row0 = 16 * ks + 4 * c;
+        const int sw = c & 2;
         const int widx[3] = {wi, w1i, w2i};
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t info_base = s_base + Lay::kInfoOff;
         const uint32_t scl_base = s_base + Lay::kSclOff;
         // What a decoder thread takes from code slot cs once it has landed:
-        // the stage's take / valid / more, this thread's 4 scales and the 3
-        // words of each of its 4 rows.  The slot is released right after.
-        struct Held { int take, valid, more; float sv[4]; uint32_t wv[4][3]; };
+        // the stage's take / valid / more, this thread's 4 scales (bf16
+        // pairs) and the 3 words of each of its 4 rows.  The slot is released
+        // right after.
+        struct Held { int take, valid, more; uint32_t s01, s23; uint32_t wv[4][3]; };
         auto take_slot = [&](int cs, Held& h) {
             const uint32_t info = info_base + (uint32_t)cs * 16u;
             uint32_t d0, d1, d2, d3, s01, s23;
@@ -269,17 +278,15 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             h.take = (int)d0;
             h.valid = (int)d1;
             h.more = (int)d2;
-            h.sv[0] = bf16_bits_to_float(s01 & 0xffffu);
-            h.sv[1] = bf16_bits_to_float(s01 >> 16);
-            h.sv[2] = bf16_bits_to_float(s23 & 0xffffu);
-            h.sv[3] = bf16_bits_to_float(s23 >> 16);
+            h.s01 = s01;
+            h.s23 = s23;
             const uint32_t tile = c_base + (uint32_t)cs * kStCBytes;
             #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 #pragma unroll
                 for (int t = 0; t < 3; ++t) {
                     uint32_t v;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + ctile_off(row0 + i, widx[t])));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + ctile_off(row0 + (i ^ sw), widx[t])));
                     h.wv[i][t] = v;
                 }
             }
@@ -303,24 +310,31 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             const bool active = ks < h0.take;
             uint32_t pk[16];
             if (active) {
-                // rows past the split enter the MMA as zeros
-                #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (row0 + i >= h0.valid) {
-                        h0.sv[i] = 0.f;
-                        h0.wv[i][0] = h0.wv[i][1] = h0.wv[i][2] = 0u;
-                    }
-                // bits [S, S + 64) of each row: the window of column t0+e at bit (7-e) k
-                uint32_t ww[4][2];
+                // bits [S, S + 64) of each row, back in row order: the window
+                // of column t0+e at bit (7-e) k
+                uint32_t wl[4][2], ww[4][2];
                 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    ww[i][0] = __funnelshift_r(h0.wv[i][0], h0.wv[i][1], off);
-                    ww[i][1] = __funnelshift_r(h0.wv[i][1], h0.wv[i][2], off);
+                    wl[i][0] = __funnelshift_r(h0.wv[i][0], h0.wv[i][1], off);
+                    wl[i][1] = __funnelshift_r(h0.wv[i][1], h0.wv[i][2], off);
+                }
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ww[i][0] = sw ? wl[i ^ 2][0] : wl[i][0];
+                    ww[i][1] = sw ? wl[i ^ 2][1] : wl[i][1];
+                }
+                // rows past the split enter the MMA as zeros (zero scale; the
+                // codebook entries are finite)
+                float sv[4];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t pr = i < 2 ? h0.s01 : h0.s23;
+                    sv[i] = row0 + i >= h0.valid ? 0.f : bf16_bits_to_float((i & 1) ? pr >> 16 : pr & 0xffffu);
                 }
                 // region r: lane g <- column t0+2r, lane g+8 <- column t0+2r+1;
                 // registers (rows 4c, 4c+1) and (rows 4c+2, 4c+3) of each
                 auto wgt = [&](int i, int e) {
-                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), h0.sv[i]);
+                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), sv[i]);
                 };
                 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -428,12 +442,14 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             }
             __syncwarp();
         }
-    } else if (warp == kStMmaWarp) {
+    } else if (warp >= kStMmaWarp) {
         // ------------------------------------------------------------ MMA issue
-        // One wait per stage: the decoders arrive on afull after they took
-        // the stage's slot, so the slot's activations have landed too.  One
-        // commit frees the A stage and one the slot.
+        // Warp 20 + r issues region r of every stage.  One wait per stage:
+        // the decoders arrive on afull after they took the stage's slot, so
+        // the slot's activations have landed too.  One commit of each of the
+        // four warps frees the A stage, one the slot.
         if (lane == 0) {
+            const int r = warp - kStMmaWarp;
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, NPAD);
             Cursor cur;
             cursor_init(sc, cur, xb, xe);
@@ -449,15 +465,14 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                 const int as = j % kStStages, cs = j % kStCStages;
                 if (!tc::mbar_wait(&afull[as], (j / kStStages) & 1, abort_flag, kStWaitNs)) break;
                 tc::tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(ic % kDBuf) * (4 * NPAD);
-                const uint32_t bsa = b_base + (uint32_t)cs * Lay::kB;
-                for (int kk = 0; kk < st.take; ++kk) {
-                    const uint64_t bd = tc::sdesc_sw128(bsa + (uint32_t)kk * 32u, 1024u);
-                    #pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        tc::mma_ts(d + (uint32_t)r * NPAD, tmem + kStACol + (uint32_t)(as * 128 + r * 32 + kk * 8), bd,
-                                   idesc, (st.first && kk == 0) ? 0u : 1u);
-                }
+                const uint32_t d = tmem + (uint32_t)((ic % kDBuf) * (4 * NPAD) + r * NPAD);
+                const uint32_t a = tmem + kStACol + (uint32_t)(as * 128 + r * 32);
+                // K step kk: 32 bytes further along the swizzled rows (the
+                // descriptor's address field counts 16-byte units)
+                const uint64_t bd = tc::sdesc_sw128(b_base + (uint32_t)cs * Lay::kB, 1024u);
+                for (int kk = 0; kk < st.take; ++kk)
+                    tc::mma_ts(d, a + (uint32_t)(kk * 8), bd + (uint64_t)(2 * kk), idesc,
+                               (st.first && kk == 0) ? 0u : 1u);
                 tc::mma_commit(&aempty[as]);
                 tc::mma_commit(&sempty[cs]);
                 if (st.last) tc::mma_commit(&dfull[ic % kDBuf]);
@@ -514,7 +529,8 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
 
     __syncthreads();
     if (warp == kStMmaWarp) {
-        // no MMA may still write tensor memory when it is released
+        // no MMA of the four issuing warps may still write tensor memory
+        // when it is released
         tc::mbar_wait(done, 0, abort_flag, kStWaitNs);
         __syncwarp();
         tc::tc_fence_after();

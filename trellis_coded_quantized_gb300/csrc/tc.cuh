@@ -48,6 +48,17 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// The same with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of the shorter
+// system-dependent time, so a warp that waits long issues almost nothing.
+__device__ __forceinline__ bool mbar_try_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall-clock time, or as soon as *abort is set by another
 // thread; returns false in both cases (and sets *abort on a timeout).
@@ -57,7 +68,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_hint(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > limit_ns) {
             *abort = 1;
