@@ -93,9 +93,12 @@ __device__ __forceinline__ void stage_lut_rep8(float* lut_s, const float* __rest
 // Programmatic dependent launch.  A kernel launched with
 // launch_pdl() may be placed on the GPU while the previous kernel of its
 // stream still runs; pdl_wait() blocks until that kernel has completed and
-// its writes are visible, so it comes before the first global-memory access.
+// its writes are visible, so it comes before the first access to memory
+// that kernel may write (activations, outputs, workspace, the status word).
+// The packed weights (codes, scales, codebook) are inputs that no kernel of
+// this library writes, so a kernel may read them before pdl_wait().
 // pdl_release() lets the next such kernel be placed.  Both are no-ops for a
-// kernel launched the ordinary way.
+// kernel launched the ordinary way (whose predecessor has then completed).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

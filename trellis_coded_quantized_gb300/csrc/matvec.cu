@@ -84,7 +84,9 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
               int rows, int units, int tg, int ng, int interleave, uint16_t* __restrict__ out) {
     extern __shared__ __align__(16) float smem[];
     pdl_release();
-    pdl_wait();
+    // The codebook, codes and scales are read before griddepcontrol.wait,
+    // while the previous kernel of the stream may still be finishing; only
+    // the activations (and the output) wait for it.
     float* lut_s = smem;                              // 8-way replicated codebook
     const int wg = tg >> 5;                           // warps per row group
     float* red = smem + kLutN * kLutRep;              // [2][ng][wg][kRB]
@@ -98,26 +100,6 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
     const int64_t wpr = block_row_stride(units / kUnitsPerBlock, kBT * K / 32, interleave);
     const uint32_t gofs = lut_rep_lane_offset();
 
-    // activations of this thread's unit as bf16 pairs: xp[j] holds windows
-    // 2j (high half) and 2j+1 (low half), i.e. columns c0+31-2j and c0+30-2j
-    uint32_t xp[16];
-    if (active) {
-        const int c0 = (t >> 3) * kBT + (224 - 32 * (t & 7));
-        const uint4* src = reinterpret_cast<const uint4*>(x + c0);
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(src + q);
-            // word e of chunk q holds columns c0+8q+2e (lo) and c0+8q+2e+1 (hi)
-            xp[15 - 4 * q] = v.x;
-            xp[14 - 4 * q] = v.y;
-            xp[13 - 4 * q] = v.z;
-            xp[12 - 4 * q] = v.w;
-        }
-    } else {
-        #pragma unroll
-        for (int j = 0; j < 16; ++j) xp[j] = 0u;
-    }
-    __syncthreads();
 
     // this CTA's (virtual) rows [r0, r1)
     const int vm = GATEUP ? 2 : 1;
@@ -153,6 +135,28 @@ matvec_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes
             for (int j = 0; j < K; ++j) pb[j] = 0u;
         }
     }
+
+    pdl_wait();
+    // activations of this thread's unit as bf16 pairs: xp[j] holds windows
+    // 2j (high half) and 2j+1 (low half), i.e. columns c0+31-2j and c0+30-2j
+    uint32_t xp[16];
+    if (active) {
+        const int c0 = (t >> 3) * kBT + (224 - 32 * (t & 7));
+        const uint4* src = reinterpret_cast<const uint4*>(x + c0);
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            // word e of chunk q holds columns c0+8q+2e (lo) and c0+8q+2e+1 (hi)
+            xp[15 - 4 * q] = v.x;
+            xp[14 - 4 * q] = v.y;
+            xp[13 - 4 * q] = v.z;
+            xp[12 - 4 * q] = v.w;
+        }
+    } else {
+        #pragma unroll
+        for (int j = 0; j < 16; ++j) xp[j] = 0u;
+    }
+    __syncthreads();
 
     int buf = 0;
     for (int j0 = 0; j0 < per_group; j0 += kRB, buf ^= 1) {

@@ -45,10 +45,10 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
                float* __restrict__ partial) {
     constexpr int RW = sc_row_warps(MB);
     extern __shared__ __align__(16) float smem[];
-    pdl_wait();                                         // x, and the partials the last reduction read
     float* lut_s = smem;                                // 8-way replicated codebook
     float* red = smem + kLutN * kLutRep;                // [RW-1][nurb][MB][32 cols][32 lanes]
-    stage_lut_rep8(lut_s, lut);
+    stage_lut_rep8(lut_s, lut);                         // a weight input: before the wait
+    pdl_wait();                                         // x, and the partials the last reduction read
     __syncthreads();
     // let the split reduction be scheduled now (it waits for this grid's
     // completion before reading anything)
@@ -284,9 +284,9 @@ scatter_mma_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __rest
                    int R, int C, int splits, int rp, int interleave, int xpitch, int rp16,
                    float* __restrict__ partial) {
     extern __shared__ __align__(16) float smem[];
-    pdl_wait();
     float* lut_s = smem;                                // 8-way replicated codebook
-    stage_lut_rep8(lut_s, lut);
+    stage_lut_rep8(lut_s, lut);                         // a weight input: before the wait
+    pdl_wait();
 
     constexpr int wpb = kBT * K / 32;
     // per warp: 2 chunks of 16 rows x (4k + 2 used) words of the tile's half
