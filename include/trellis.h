@@ -146,6 +146,27 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
                                const trellis_geometry* g, void* out, void* stream);
 
 /*
+ * The gate and up projections of one SwiGLU MLP layer at 1 <= M <= 32 in
+ * one launch, with the SiLU gate applied on the way out (the pages' MLP
+ * input is the RMSNorm output, tiled-prefill.ts; the fused chain is this
+ * library's).  Both matrices have geometry g (axis 1: rows = intermediate
+ * width, cols = hidden width) and share the codebook lut.
+ *   x            bf16 [M, cols], 16-byte aligned
+ *   gate_codes, up_codes (16-byte aligned), gate_scales, up_scales: the two
+ *                packed matrices
+ *   h_out        bf16 [M, rows]  h[m][r] = bf16( silu(gate[m][r]) * up[m][r] ),
+ *                gate and up each what trellis_prefill gives, silu(v) =
+ *                v / (1 + e^-v) in fp32: bit for bit trellis_prefill twice
+ *                followed by trellis_silu_mul
+ * Requires g->axis == 1; the rounded contract only (TRELLIS_FLAG_UNROUNDED
+ * is TRELLIS_ERR_GEOMETRY, as for trellis_prefill).
+ */
+trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t* gate_codes,
+                                       const void* gate_scales, const uint32_t* up_codes,
+                                       const void* up_scales, const float* lut,
+                                       const trellis_geometry* g, void* h_out, void* stream);
+
+/*
  * Axis-0 scatter for 1 <= M <= 32 activation rows (scatter.ts: scatter
  * kernels, launch and the sum over splits).  The rows are cut into `splits`
  * ranges of rp = ceil(rows/splits) rows; range s covers

@@ -180,6 +180,20 @@ def test_gate_up_validation(lib):
     assert f(_p(U), _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(gu), _p(A), None) == ALIGN
 
 
+def test_gate_up_prefill_validation(lib):
+    g1 = geometry(1, 256, 512, 2)
+    g0 = geometry(0, 256, 512, 2)
+    f = lib.trellis_gate_up_prefill
+    assert f(_p(A), 8, _p(A), _p(A), None, _p(A), _p(A), ctypes.byref(g1), _p(A), None) == NULL
+    assert f(_p(A), 8, _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(g0), _p(A), None) == SHAPE
+    for M in (0, 33):
+        assert f(_p(A), M, _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == SHAPE
+    assert f(_p(A), 8, _p(A), _p(A), _p(U), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    assert f(_p(U), 8, _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(g1), _p(A), None) == ALIGN
+    gu = geometry(1, 256, 512, 2, unrounded=True)
+    assert f(_p(A), 8, _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(gu), _p(A), None) == GEOM
+
+
 def test_product_path_never_uses_the_oracle():
     """The package and its CUDA sources neither import, include, link nor call
     the oracle (it is test infrastructure only)."""

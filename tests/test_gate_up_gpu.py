@@ -91,3 +91,53 @@ def test_gate_up_errors():
         tcq.trellis_gate_up_matvec(xw, big, ws, big, ws, l, wide)
     assert e.value.status == 3
     assert tcq.trellis_gate_up_matvec(x, c, s, c, s, l, g1).shape == (256,)
+
+
+@pytest.mark.parametrize("M,rows,cols,k,interleave", [
+    (16, 17408, 5120, 3, 0),         # the MLP layer's gate/up geometry at M = 16
+    (32, 17408, 5120, 4, 0),
+    (5, 17408, 5120, 2, 0),
+    (2, 300, 1024, 2, 2),            # two CTAs of 128 rows and a ragged one
+    (17, 1000, 2304, 4, 0),          # N = 32, 9 column blocks, ragged rows
+    (1, 129, 512, 3, 0),             # one row past a 128-row tile
+    (32, 37, 256, 2, 0),             # one block, one partial tile
+])
+def test_gate_up_prefill_equals_prefills_then_silu(orc, M, rows, cols, k, interleave):
+    """trellis_gate_up_prefill is bit for bit trellis_prefill twice and
+    trellis_silu_mul; the chain's projections agree with the oracle."""
+    pg = synth.problem(1, M, rows, cols, k, seed=41)
+    pu = synth.problem(1, M, rows, cols, k, seed=42)
+    lut = pg["lut"]
+    cg, cu = pg["codes"], pu["codes"]
+    if interleave == 2:
+        cg, cu = _inter(cg, rows, cols, k), _inter(cu, rows, cols, k)
+    g = tcq.geometry(1, rows, cols, k, interleave)
+    x = dev(pg["x"])
+    dcg, dsg, dcu, dsu, dl = dev(cg), dev(pg["scales"]), dev(cu), dev(pu["scales"]), dev(lut)
+    h = tcq.trellis_gate_up_prefill(x, dcg, dsg, dcu, dsu, dl, g)
+    gate = tcq.trellis_prefill(x, dcg, dsg, dl, g)
+    up = tcq.trellis_prefill(x, dcu, dsu, dl, g)
+    h_chain = tcq.trellis_silu_mul(gate, up)
+    assert h.shape == (M, rows)
+    assert np.array_equal(host_bf16(h), host_bf16(h_chain)), "fused output differs from prefill, prefill, silu_mul"
+    assert tcq.trellis_device_status() == 0
+    if rows * cols <= 2304 * 1000:       # the oracle on the small geometries
+        for p, got in ((pg, gate), (pu, up)):
+            w, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], lut)
+            y, a, _ = orc.matmul_axis1(pg["x"], w)
+            check_close(orc, host_bf16(got), y, a, f"gate/up prefill projection {rows}x{cols} k={k} M={M}")
+        ref = orc.silu_mul(host_bf16(gate), host_bf16(up))
+        assert np.all(_ulps(host_bf16(h), ref) <= 1.0)
+
+
+def test_gate_up_prefill_errors():
+    p = synth.problem(1, 4, 256, 512, 2, seed=43)
+    g0 = tcq.geometry(0, 256, 512, 2)
+    gu = tcq.geometry(1, 256, 512, 2, unrounded=True)
+    x, c, s, l = dev(p["x"]), dev(p["codes"]), dev(p["scales"]), dev(p["lut"])
+    with pytest.raises(tcq.TrellisError) as e:
+        tcq.trellis_gate_up_prefill(x, c, s, c, s, l, g0)
+    assert e.value.status == 3
+    with pytest.raises(tcq.TrellisError) as e:
+        tcq.trellis_gate_up_prefill(x, c, s, c, s, l, gu)
+    assert e.value.status == 2

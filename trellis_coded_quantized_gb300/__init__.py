@@ -140,6 +140,22 @@ def trellis_prefill(x, codes, scales, lut, g, out=None, stream=None):
     return out
 
 
+def trellis_gate_up_prefill(x, gate_codes, gate_scales, up_codes, up_scales, lut, g, out=None, stream=None):
+    """Axis 1, 1 <= M <= 32, gate and up projections of one SwiGLU layer
+    (geometry g, one codebook) in one launch: x bf16 [M, cols] -> h bf16
+    [M, rows], h = bf16(silu(gate) * up), bit for bit two trellis_prefill
+    calls and trellis_silu_mul."""
+    cg, sg, t = _packed(gate_codes, gate_scales, lut, g)
+    cu, su, _ = _packed(up_codes, up_scales, lut, g)
+    M = x.shape[0]
+    xp = _dev(x, "x", _bf16_types(), (M, g.cols))
+    out = _out(out, (M, g.rows), x)
+    op = _dev(out, "out", _bf16_types(), (M, g.rows))
+    _check(_lib.load().trellis_gate_up_prefill(xp, M, cg, sg, cu, su, t, ctypes.byref(g), op, _stream(stream)),
+           "trellis_gate_up_prefill")
+    return out
+
+
 def trellis_scatter_workspace_bytes(g, M: int, splits: int = 0) -> int:
     return int(_lib.load().trellis_scatter_workspace_bytes(ctypes.byref(g), M, splits))
 

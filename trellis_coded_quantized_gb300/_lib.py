@@ -11,7 +11,7 @@ LIB_PATH = os.path.join(HERE, "libtrellis.so")
 
 # the entry points declared in include/trellis.h
 EXPORTS = (
-    "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_scatter", "trellis_scatter_f32",
+    "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_gate_up_prefill", "trellis_scatter", "trellis_scatter_f32",
     "trellis_round_bf16", "trellis_scatter_noalloc",
     "trellis_scatter_workspace_bytes",
     "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_gather_probe",
@@ -42,6 +42,7 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         "trellis_matvec": ([P, P, P, P, G, P, P], I32),
         "trellis_gate_up_matvec": ([P, P, P, P, P, P, G, P, P], I32),
         "trellis_prefill": ([P, I32, P, P, P, G, P, P], I32),
+        "trellis_gate_up_prefill": ([P, I32, P, P, P, P, P, G, P, P], I32),
         "trellis_scatter": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
         "trellis_scatter_f32": ([P, I32, P, P, P, G, I32, P, SZ, P, P], I32),
         "trellis_round_bf16": ([P, I64, P, P], I32),

@@ -152,6 +152,23 @@ trellis_status trellis_prefill(const void* x, int32_t M, const uint32_t* codes,
                                         static_cast<cudaStream_t>(stream)));
 }
 
+trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t* gate_codes,
+                                      const void* gate_scales, const uint32_t* up_codes, const void* up_scales,
+                                      const float* lut, const trellis_geometry* g, void* h_out, void* stream) {
+    if (!x || !gate_codes || !gate_scales || !up_codes || !up_scales || !lut || !g || !h_out)
+        return TRELLIS_ERR_NULL;
+    trellis_status st = check_geometry(g, 1, false);
+    if (st != TRELLIS_OK) return st;
+    if (M < 1 || M > 32) return TRELLIS_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gate_codes) || !aligned16(up_codes) || !aligned16(lut)) return TRELLIS_ERR_ALIGN;
+    const DeviceFacts* d;
+    if ((st = current_device(&d)) != TRELLIS_OK) return st;
+    return launched(tcq::launch_gate_up_prefill(packed(gate_codes, gate_scales, lut, g), up_codes,
+                                                static_cast<const uint16_t*>(up_scales),
+                                                static_cast<const uint16_t*>(x), M, static_cast<uint16_t*>(h_out),
+                                                d->status, d->sm_count, static_cast<cudaStream_t>(stream)));
+}
+
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {
     if (check_geometry(g, -1, true) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
     const bool unr = (g->flags & TRELLIS_FLAG_UNROUNDED) != 0;

@@ -33,6 +33,11 @@ cudaError_t launch_gate_up_matvec(const Packed& gate, const uint32_t* up_codes, 
 // axis 1, M in 1..32, tensor cores
 cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* out,
                            int* status, int sm_count, cudaStream_t stream);
+// The gate and up projections (same geometry, codebook of `gate`) at
+// M = 1..32 in one launch: h[m][r] = bf16(silu(gate[m][r]) * up[m][r]).
+cudaError_t launch_gate_up_prefill(const Packed& gate, const uint32_t* up_codes, const uint16_t* up_scales,
+                                   const uint16_t* x, int M, uint16_t* h, int* status, int sm_count,
+                                   cudaStream_t stream);
 
 // axis 0: partials [M, splits, cols] then the split reduction into out [M, cols]
 // out is bf16 [M, cols], or with out_f32 the unrounded f32 sums [M, cols]

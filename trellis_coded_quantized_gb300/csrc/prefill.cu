@@ -118,17 +118,21 @@ __device__ __forceinline__ void read_quarter(uint32_t* w, const uint8_t* row, in
     w[kPfUnits * K] = reinterpret_cast<const uint32_t*>(row)[nb];
 }
 
-template <int K, int NPAD>
+// GU: the gate and up projections of a SwiGLU layer in one launch.  The CTA
+// walks the column blocks of its gate rows, then those of the same up rows
+// (2 x nblocks blocks through the same pipeline, the codes and scales of the
+// second pass from codes_u / scales_u), accumulating into two tensor-memory
+// accumulators, and its epilogue writes h = bf16(silu(bf16(gate)) *
+// bf16(up)) -- the bits trellis_prefill twice and trellis_silu_mul give.
+template <int K, int NPAD, bool GU>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict__ codes,
-               const uint16_t* __restrict__ scales, const float* __restrict__ lut,
+               const uint16_t* __restrict__ scales, const uint32_t* __restrict__ codes_u,
+               const uint16_t* __restrict__ scales_u, const float* __restrict__ lut,
                int rows, int cols, int interleave, int tile_rows, uint16_t* __restrict__ out,
                int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ uint8_t smem_raw[];
-    // a programmatic dependent of the previous kernel: nothing is read,
-    // written or allocated (tensor memory) before that kernel has completed
-    pdl_wait();
     pdl_release();
     // 1024-byte aligned base, derived by pointer arithmetic on the shared
     // array (an integer round trip would lose the shared address space and
@@ -146,7 +150,12 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the codebook (a weight input, never written by this library) is staged
+    // while the previous kernel of the stream may still run; nothing else is
+    // read, written or allocated (tensor memory) before that kernel has
+    // completed
     stage_lut_rep8(lut_s, lut);
+    pdl_wait();
     if (threadIdx.x == 0) {
         for (int st = 0; st < kPfAStages; ++st) {
             tc::mbar_init(&full[st], kPfDecWarps * 32 + 32);
@@ -170,6 +179,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     const uint32_t tmem = *tmem_slot;
 
     const int nblocks = cols / kBT;
+    const int nbt = GU ? 2 * nblocks : nblocks;      // blocks through the pipeline
     constexpr int wpb = Lay::kWpb;
     // this CTA owns tile_rows (<= 128) rows: the MMA always spans 128 lanes,
     // lanes past the CTA's rows decode nothing and are not stored
@@ -181,10 +191,12 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const int q = warp & 3, part = warp >> 2;
         const int rl = 32 * q + lane;
         const bool valid = rl < nvalid;
-        const float s = valid ? bf16_bits_to_float(__ldg(scales + row0 + rl)) : 0.f;
+        const float s_g = valid ? bf16_bits_to_float(__ldg(scales + row0 + rl)) : 0.f;
+        const float s_u = GU && valid ? bf16_bits_to_float(__ldg(scales_u + row0 + rl)) : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t gofs = lut_rep_lane_offset();
-        for (int b = 0; b < nblocks; ++b) {
+        for (int b = 0; b < nbt; ++b) {
+            const float s = GU && b >= nblocks ? s_u : s_g;
             const int stage = b % kPfAStages, use = b / kPfAStages;
             const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
             if (!tc::mbar_wait(&cfull[cst], cuse & 1, abort_flag, kWaitLimitNs)) break;
@@ -229,12 +241,14 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const int64_t wpr = block_row_stride(nblocks, wpb, interleave);
         constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
         const int nchunks = nvalid * cpr;
-        for (int b = 0; b < nblocks; ++b) {
+        for (int b = 0; b < nbt; ++b) {
             const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
             if (b >= kPfCodeStages &&
                 !tc::mbar_wait(&cempty[cst], (cuse - 1) & 1, abort_flag, kWaitLimitNs)) break;
             const uint32_t ct = tc::smem_addr(cs + cst * Lay::kCodeStage);
-            const uint32_t* src0 = codes + (int64_t)row0 * wpr + block_col_base(b, rows, wpb, interleave);
+            const bool upm = GU && b >= nblocks;
+            const uint32_t* src0 = (upm ? codes_u : codes) + (int64_t)row0 * wpr +
+                                   block_col_base(upm ? b - nblocks : b, rows, wpb, interleave);
             for (int c = lane; c < nchunks; c += 32) {
                 const int r = c / cpr, part = c - (c / cpr) * cpr;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
@@ -256,10 +270,11 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         // zero-filled); the warp waits for its own copies, then fences them
         // into the async proxy before arriving on full[stage].
         const uint32_t xs_base = tc::smem_addr(xs);
-        for (int b = 0; b < nblocks; ++b) {
+        for (int b = 0; b < nbt; ++b) {
             const int stage = b % kPfAStages, use = b / kPfAStages;
             if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
             __syncwarp();
+            const int bb = GU && b >= nblocks ? b - nblocks : b;   // column block
             const uint32_t st = xs_base + stage * Lay::kXStage;
             #pragma unroll 8
             for (int qd = lane; qd < NPAD * 32; qd += 32) {
@@ -267,7 +282,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 const int kc = cc >> 3, c = cc & 7;
                 const uint32_t dst = st + kc * Lay::kXChunk + n * 128 + ((c ^ (n & 7)) << 4);
                 const bool in = n < M;
-                const uint16_t* src = in ? x + (int64_t)n * cols + (int64_t)b * kBT + cc * 8 : x;
+                const uint16_t* src = in ? x + (int64_t)n * cols + (int64_t)bb * kBT + cc * 8 : x;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
                              :: "r"(dst), "l"(src), "r"(in ? 16 : 0) : "memory");
             }
@@ -280,16 +295,19 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, NPAD);
             const uint32_t xs_base = tc::smem_addr(xs);
-            for (int b = 0; b < nblocks; ++b) {
+            for (int b = 0; b < nbt; ++b) {
                 const int stage = b % kPfAStages;
                 if (!tc::mbar_wait(&full[stage], (b / kPfAStages) & 1, abort_flag, kWaitLimitNs)) break;
                 tc::tc_fence_after();
+                const bool upm = GU && b >= nblocks;
+                const int bb = upm ? b - nblocks : b;
+                const uint32_t dcol = tmem + kDCol + (upm ? (uint32_t)NPAD : 0u);
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const uint32_t a = tmem + a_col(stage) + (uint32_t)(8 * j);
                     const uint64_t bd = tc::sdesc_sw128(
                         xs_base + stage * Lay::kXStage + (j >> 2) * Lay::kXChunk + (j & 3) * 32, 1024);
-                    tc::mma_ts(tmem + kDCol, a, bd, idesc, (b | j) != 0 ? 1u : 0u);
+                    tc::mma_ts(dcol, a, bd, idesc, (bb | j) != 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&empty[stage]);
             }
@@ -308,14 +326,22 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + kDCol;
         #pragma unroll
         for (int c = 0; c < NPAD; c += 16) {
-            uint32_t d[16];
+            uint32_t d[16], du[16];
             tc::tmem_ld16(taddr + c, d);
+            if constexpr (GU) tc::tmem_ld16(taddr + NPAD + c, du);
             tc::tmem_wait_ld();
             if (ok && !*abort_flag && rl < nvalid) {
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c + j;
-                    if (n < M) out[(int64_t)n * rows + row] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(d[j])));
+                    if (n >= M) continue;
+                    uint16_t v = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(d[j])));
+                    if constexpr (GU) {
+                        const uint16_t u = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(du[j])));
+                        v = __bfloat16_as_ushort(__float2bfloat16_rn(
+                            silu_mul_f32(bf16_bits_to_float(v), bf16_bits_to_float(u))));
+                    }
+                    out[(int64_t)n * rows + row] = v;
                 }
             }
         }
@@ -329,11 +355,11 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     if (threadIdx.x == 0 && *abort_flag) atomicOr(status, kStatusWaitTimeout);
 }
 
-template <int K, int NPAD>
-cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, int* status,
-                      int sm_count, cudaStream_t stream) {
+template <int K, int NPAD, bool GU>
+cudaError_t launch_kn(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x, int M,
+                      uint16_t* out, int* status, int sm_count, cudaStream_t stream) {
     const int smem = PfLayout<K, NPAD>::kAlloc;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<K, NPAD>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<K, NPAD, GU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // Between 64 and 128 rows per SM: spread the rows over all SMs (the decode
@@ -342,29 +368,41 @@ cudaError_t launch_kn(const Packed& p, const uint16_t* x, int M, uint16_t* out, 
     if (sm_count > 0 && p.rows > (int64_t)64 * sm_count && p.rows <= (int64_t)kPfRows * sm_count)
         tile_rows = (int)((p.rows + sm_count - 1) / sm_count);
     const unsigned grid = (unsigned)((p.rows + tile_rows - 1) / tile_rows);
-    e = launch_pdl(prefill_kernel<K, NPAD>, dim3(grid), dim3(kPfThreads), (size_t)smem, stream, x, M, p.codes,
-                   p.scales, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status);
+    e = launch_pdl(prefill_kernel<K, NPAD, GU>, dim3(grid), dim3(kPfThreads), (size_t)smem, stream, x, M, p.codes,
+                   p.scales, codes_u, scales_u, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int K>
-cudaError_t launch_k(const Packed& p, const uint16_t* x, int M, uint16_t* out, int* status,
-                     int sm_count, cudaStream_t stream) {
-    if (M <= 16) return launch_kn<K, 16>(p, x, M, out, status, sm_count, stream);
-    return launch_kn<K, 32>(p, x, M, out, status, sm_count, stream);
+template <int K, bool GU>
+cudaError_t launch_k(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x, int M,
+                     uint16_t* out, int* status, int sm_count, cudaStream_t stream) {
+    if (M <= 16) return launch_kn<K, 16, GU>(p, codes_u, scales_u, x, M, out, status, sm_count, stream);
+    return launch_kn<K, 32, GU>(p, codes_u, scales_u, x, M, out, status, sm_count, stream);
+}
+
+template <bool GU>
+cudaError_t launch_any(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x, int M,
+                       uint16_t* out, int* status, int sm_count, cudaStream_t stream) {
+    switch (p.k) {
+        case 2: return launch_k<2, GU>(p, codes_u, scales_u, x, M, out, status, sm_count, stream);
+        case 3: return launch_k<3, GU>(p, codes_u, scales_u, x, M, out, status, sm_count, stream);
+        case 4: return launch_k<4, GU>(p, codes_u, scales_u, x, M, out, status, sm_count, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const Packed& p, const uint16_t* x, int M, uint16_t* out,
                            int* status, int sm_count, cudaStream_t stream) {
-    switch (p.k) {
-        case 2: return launch_k<2>(p, x, M, out, status, sm_count, stream);
-        case 3: return launch_k<3>(p, x, M, out, status, sm_count, stream);
-        case 4: return launch_k<4>(p, x, M, out, status, sm_count, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_any<false>(p, nullptr, nullptr, x, M, out, status, sm_count, stream);
+}
+
+cudaError_t launch_gate_up_prefill(const Packed& gate, const uint32_t* up_codes, const uint16_t* up_scales,
+                                   const uint16_t* x, int M, uint16_t* h, int* status, int sm_count,
+                                   cudaStream_t stream) {
+    return launch_any<true>(gate, up_codes, up_scales, x, M, h, status, sm_count, stream);
 }
 
 }  // namespace tcq

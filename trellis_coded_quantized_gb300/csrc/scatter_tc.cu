@@ -176,9 +176,6 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
     constexpr int kDBuf = st_dbufs(NPAD);
     static_assert(kDBuf * 4 * NPAD <= (int)kStACol, "D buffers overlap the A stages");
     extern __shared__ uint8_t smem_raw[];
-    // nothing is read, written or allocated before the previous kernel of
-    // the stream has completed
-    pdl_wait();
     pdl_release();
     uint8_t* base = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
     float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
@@ -203,7 +200,12 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
     static_assert(Lay::kSclOff % 128 == 0 && kStSclBytes % 128 == 0, "TMA destinations must be 128-byte aligned");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the codebook (a weight input, never written by this library) is staged
+    // while the previous kernel of the stream may still run; nothing else is
+    // read, written or allocated (tensor memory) before that kernel has
+    // completed
     stage_lut_rep8(lut_s, lut);
+    pdl_wait();
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStStages; ++i) {
             tc::mbar_init(&afull[i], kStDecWarps * 32);

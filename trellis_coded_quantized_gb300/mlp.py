@@ -8,11 +8,10 @@ SwiGLU chain is the plain reading of "Qwen's MLP geometry"):
     x' = down(h)                    axis 0, intermediate -> hidden
 Without a residual.  Layer l, matrix j (0 gate, 1 up, 2 down) is drawn with
 seed 1000*l + j; all matrices share one codebook (the pages' codebook is one
-fixed function of the window), drawn with seed CODEBOOK_SEED.  M = 1 runs
-gate, up and silu*up as one trellis_gate_up_matvec, M >= 2 two
-trellis_prefill launches and trellis_silu_mul; down always uses
-trellis_scatter (split count by M, see splits_for).  Every step runs in
-libtrellis kernels.
+fixed function of the window), drawn with seed CODEBOOK_SEED.  Gate, up and
+silu*up run as one launch: trellis_gate_up_matvec at M = 1,
+trellis_gate_up_prefill at M >= 2; down always uses trellis_scatter (split
+count by M, see splits_for).  Every step runs in libtrellis kernels.
 """
 from __future__ import annotations
 
@@ -77,10 +76,9 @@ class PackedMLPStack:
         return len(self.layers) * 3 * self.inter * self.hidden * self.k // 8
 
     def launches_per_pass(self, M: int) -> int:
-        # rmsnorm; gate+up+silu fused (M = 1) or gate, up, silu*up; the
-        # scatter (one FMA pass up to 2 rows, one tensor-core pass from 3);
-        # the split reduction
-        return len(self.layers) * (1 + (1 if M == 1 else 3) + 1 + 1)
+        # rmsnorm; gate+up+silu fused; the scatter (one FMA pass up to 2
+        # rows, one tensor-core pass from 3); the split reduction
+        return len(self.layers) * (1 + 1 + 1 + 1)
 
     def layer(self, l: int, x, out, keep=None):
         """One layer on x [M, hidden] into out [M, hidden]."""
@@ -95,9 +93,11 @@ class PackedMLPStack:
                 tcq.trellis_matvec(n[0], gate["codes"], gate["scales"], self.lut, gate["g"], out=g[0])
                 tcq.trellis_matvec(n[0], up["codes"], up["scales"], self.lut, up["g"], out=u[0])
         else:
-            tcq.trellis_prefill(n, gate["codes"], gate["scales"], self.lut, gate["g"], out=g)
-            tcq.trellis_prefill(n, up["codes"], up["scales"], self.lut, up["g"], out=u)
-            tcq.trellis_silu_mul(g, u, out=h)
+            tcq.trellis_gate_up_prefill(n, gate["codes"], gate["scales"], up["codes"], up["scales"], self.lut,
+                                        gate["g"], out=h)
+            if keep is not None:        # the two projections on their own, for stage checks
+                tcq.trellis_prefill(n, gate["codes"], gate["scales"], self.lut, gate["g"], out=g)
+                tcq.trellis_prefill(n, up["codes"], up["scales"], self.lut, up["g"], out=u)
         tcq.trellis_scatter(h, down["codes"], down["scales"], self.lut, down["g"], splits=self.splits_for(M),
                             workspace=self.ws, out=out)
         if keep is not None:
