@@ -181,20 +181,25 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     const int nblocks = cols / kBT;
     const int nbt = GU ? 2 * nblocks : nblocks;      // blocks through the pipeline
     constexpr int wpb = Lay::kWpb;
-    // this CTA owns tile_rows (<= 128) rows: the MMA always spans 128 lanes,
-    // lanes past the CTA's rows decode nothing and are not stored
+    // this CTA owns tile_rows (<= 128) rows: the MMA always spans 128 lanes.
+    // Its nvalid rows are dealt evenly to the 4 lane quarters (rpq each, the
+    // last quarter fewer), so every decoder warp has about the same work;
+    // local row q*rpq + i sits in lane 32q + i, and lanes past rpq decode
+    // nothing and are not stored.
     const int row0 = blockIdx.x * tile_rows;
     const int nvalid = min(tile_rows, rows - row0);
+    const int rpq = (nvalid + 3) >> 2;
 
     if (warp < kPfDecWarps) {
         // ------------------------------------------------------------ decoders
         const int q = warp & 3, part = warp >> 2;
-        const int rl = 32 * q + lane;
-        const bool valid = rl < nvalid;
+        const int rl = q * rpq + lane;
+        const bool valid = lane < rpq && rl < nvalid;
         const float s_g = valid ? bf16_bits_to_float(__ldg(scales + row0 + rl)) : 0.f;
         const float s_u = GU && valid ? bf16_bits_to_float(__ldg(scales_u + row0 + rl)) : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        const uint32_t gofs = lut_rep_lane_offset();
+        // shared address of this lane's codebook copy (entry e at +32 e)
+        const uint32_t lut_sa = tc::smem_addr(lut_s) + lut_rep_lane_offset();
         for (int b = 0; b < nbt; ++b) {
             const float s = GU && b >= nblocks ? s_u : s_g;
             const int stage = b % kPfAStages, use = b / kPfAStages;
@@ -214,12 +219,17 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 for (int j = 0; j <= K; ++j) w[j] = cw[uu * K + j];   // neighbour is the next unit's first word
                 uint32_t r[16];
                 if (valid) {                                // lanes past the CTA's rows issue no gathers
+                    // all 32 gathers of the unit are issued before the first
+                    // is used (one load-pipe round trip per unit, not several)
+                    uint32_t v[32];
                     #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float lo = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - 2 * j) | gofs);
-                        const float hi = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 30 - 2 * j) | gofs);
-                        r[j] = pack_bf16x2(__fmul_rn(lo, s), __fmul_rn(hi, s));
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j])
+                                     : "r"(lut_sa + win_off_sh<K, kLutRepShift>(w, 31 - j)));
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * j]), s),
+                                           __fmul_rn(__uint_as_float(v[2 * j + 1]), s));
                 } else {
                     #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = 0u;
@@ -321,7 +331,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const bool ok = tc::mbar_wait(done, 0, abort_flag, kWaitLimitNs);
         __syncwarp();
         tc::tc_fence_after();
-        const int rl = 32 * warp + lane;
+        const int rl = warp * rpq + lane;
         const int row = row0 + rl;
         const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + kDCol;
         #pragma unroll
@@ -330,7 +340,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
             tc::tmem_ld16(taddr + c, d);
             if constexpr (GU) tc::tmem_ld16(taddr + NPAD + c, du);
             tc::tmem_wait_ld();
-            if (ok && !*abort_flag && rl < nvalid) {
+            if (ok && !*abort_flag && lane < rpq && rl < nvalid) {
                 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c + j;

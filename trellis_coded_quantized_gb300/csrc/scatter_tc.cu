@@ -243,7 +243,8 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
         // ------------------------------------------------------------ decoders
         const int q = warp & 3, ks = warp >> 2;
         const int g = lane >> 2, c = lane & 3;
-        const uint32_t gofs = lut_rep_lane_offset();
+        // shared address of this lane's codebook copy (entry e at +32 e)
+        const uint32_t lut_sa = tc::smem_addr(lut_s) + lut_rep_lane_offset();
         // columns t0 .. t0+7 of the block; the window of column t0+e starts at
         // bit (255 - t0 - e) k = S + (7 - e) k, S = (248 - t0) k
         const int t0 = 64 * q + 8 * g;
@@ -333,11 +334,21 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                     const uint32_t pr = i < 2 ? h0.s01 : h0.s23;
                     sv[i] = row0 + i >= h0.valid ? 0.f : bf16_bits_to_float((i & 1) ? pr >> 16 : pr & 0xffffu);
                 }
+                // All 32 codebook gathers are issued before the first is used:
+                // under a busy load pipe one round trip takes hundreds of
+                // cycles, and a thread that waits on a few gathers at a time
+                // pays it several times per stage.
+                uint32_t vb[4][8];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    #pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(vb[i][e])
+                                     : "r"(lut_sa + win_off_sh<K, kLutRepShift>(ww[i], 7 - e)));
+                }
                 // region r: lane g <- column t0+2r, lane g+8 <- column t0+2r+1;
                 // registers (rows 4c, 4c+1) and (rows 4c+2, 4c+3) of each
-                auto wgt = [&](int i, int e) {
-                    return __fmul_rn(lut_at(lut_s, win_off_sh<K, kLutRepShift>(ww[i], 7 - e) | gofs), sv[i]);
-                };
+                auto wgt = [&](int i, int e) { return __fmul_rn(__uint_as_float(vb[i][e]), sv[i]); };
                 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     pk[4 * r + 0] = pack_bf16x2(wgt(0, 2 * r), wgt(1, 2 * r));
