@@ -407,6 +407,42 @@ def gather_floor_s(weights: float, rates: dict, sm: int, sm_mhz) -> float:
     return weights / (r["per_sm_per_clock"] * sm * mhz * 1e6)
 
 
+def kv_lines(torch, tcq, device, stream, hbm):
+    """The TurboQuant packed K/V decode (the second workload): the pages'
+    measured regime (D 256, 8-bit keys, 3-bit values, f16 scales, groups of
+    32) at B1 H4 N65536, joint decode (f32 values) and the inverse-256
+    rotation (bf16 values), plus a D 128 4-bit/4-bit joint decode.  Inputs
+    and outputs together are larger than L2.  Bytes are the arrays read and
+    written once."""
+    from trellis_coded_quantized_gb300 import synth
+    out = {}
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+    for name, rows, D, kb, vb, inverse in (("kv_decode_D256_k8v3", 4 * 65536, 256, 8, 3, False),
+                                           ("kv_inverse256_D256_k8v3", 4 * 65536, 256, 8, 3, True),
+                                           ("kv_decode_D128_k4v4", 4 * 131072, 128, 4, 4, False)):
+        c = synth.kv_cache(11, rows, D, kb, vb)
+        g = tcq.kv_geometry(rows, D, kb, vb, value_out_bf16=inverse)
+        args = [dev(c[n]) for n in ("kp", "ks", "kz", "vp", "vs", "centroids")]
+        signs = dev(c["signs"])
+        ko = torch.empty((rows, D), dtype=torch.bfloat16, device=device)
+        vo = torch.empty((rows, D), dtype=torch.bfloat16 if inverse else torch.float32, device=device)
+        if inverse:
+            fn = lambda i: tcq.trellis_kv_decode_inverse256(*args, signs, g, ko, vo)
+        else:
+            fn = lambda i: tcq.trellis_kv_decode(*args, g, ko, vo)
+        tb, _ = time_launches(torch, fn, 50, 3, stream, lambda: None, per_launch=False)
+        tb = tb * 1e-3 / 50
+        nbytes = sum(a.numel() * a.element_size() for a in args) + ko.numel() * 2 + vo.numel() * vo.element_size()
+        out[name] = {"us_back_to_back": round(tb * 1e6, 2), "rows": rows, "bytes": nbytes,
+                     "gbs": round(nbytes / tb / 1e9, 1), "frac_of_hbm": round(nbytes / tb / 1e9 / hbm, 4)}
+        del args, ko, vo
+        torch.cuda.empty_cache()
+    return out
+
+
 def secondary(torch, tcq, device, stream, peaks, l2, rates, sm, sm_mhz):
     """Launch times of the other configurations (context figures): `us` is
     the median of launches each bracketed by events, `us_back_to_back` the
@@ -448,6 +484,7 @@ def secondary(torch, tcq, device, stream, peaks, l2, rates, sm, sm_mhz):
         out[key] = rec
         del wl
         torch.cuda.empty_cache()
+    out.update(kv_lines(torch, tcq, device, stream, hbm))
     # the 40-layer MLP stack, M = 1 and 16
     from trellis_coded_quantized_gb300.mlp import PackedMLPStack
     stack = PackedMLPStack(layers=40, k=3, device=device, m_max=16)

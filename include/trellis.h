@@ -283,6 +283,71 @@ trellis_status trellis_silu_mul(const void* g, const void* u, int64_t n,
                                 void* out, void* stream);
 
 /*
+ * TurboQuant packed K/V cache decode (@mlx-bun/inference 1.0.0,
+ * kernels/turboquant/decode.ts, joint K/V decode kernel; inverse.ts, the
+ * decode with the inverse 256-point rotation).  A second packed-decode
+ * workload beside the trellis matmul; it shares no code path with it.
+ *
+ * The cache is `rows` positions (B * H * N of the pages' [B, H, N, D]
+ * arrays), every array row-major and contiguous:
+ *   key_codes     u8  [rows, D*key_bits/8]   code of column c at bit offset
+ *                 c*key_bits of the row's bytes, low bits first, reaching
+ *                 into the next byte when it straddles two; an 8-bit code is
+ *                 a signed byte (int8)
+ *   key_scales, key_zeros   [rows, D/key_group] of their trellis_dtype
+ *   value_codes   u8  [rows, D*value_bits/8]  same bit layout, unsigned
+ *   value_scales  [rows, D/value_group] of its trellis_dtype
+ *   centroids     f32 [1 << value_bits]
+ *   keys_out      bf16 [rows, D]   bf16( (f32(code) + f32(zero)) * f32(scale) ),
+ *                 the zero added before scaling, both in f32
+ *   values_out    f32 or bf16 [rows, D]   f32(centroids[code]) * f32(scale),
+ *                 rounded to bf16 when value_out_bf16 (the pages' deferred
+ *                 rotation)
+ * key_codes, value_codes, keys_out and values_out must be 16-byte aligned;
+ * scales and zeros aligned to their element; the codes and scales are read
+ * after the previous kernel of the stream completed, the centroids (and the
+ * signs below) before -- they are constant tables.
+ */
+typedef enum trellis_dtype {
+    TRELLIS_DT_F32 = 0,
+    TRELLIS_DT_F16 = 1,
+    TRELLIS_DT_BF16 = 2
+} trellis_dtype;
+
+typedef struct trellis_kv_geometry {
+    int64_t rows;                /* >= 1 */
+    int32_t head_dim;            /* D: 64, 128, 256 or 512 */
+    int32_t key_bits;            /* 2, 4, 5 or 8 */
+    int32_t value_bits;          /* 2, 3, 4, 5 or 8 */
+    int32_t key_group;           /* columns per key scale and zero: 32 or 64 */
+    int32_t value_group;         /* columns per value scale: 32 or 64 */
+    int32_t key_scale_dtype;     /* trellis_dtype */
+    int32_t key_zero_dtype;      /* trellis_dtype */
+    int32_t value_scale_dtype;   /* trellis_dtype */
+    int32_t value_out_bf16;      /* 0: f32 values, 1: bf16 values */
+} trellis_kv_geometry;
+
+/* Joint decode of keys and values.  A field outside the sets above is
+ * TRELLIS_ERR_GEOMETRY. */
+trellis_status trellis_kv_decode(const uint8_t* key_codes, const void* key_scales, const void* key_zeros,
+                                 const uint8_t* value_codes, const void* value_scales, const float* centroids,
+                                 const trellis_kv_geometry* g, void* keys_out, void* values_out, void* stream);
+
+/* The decode followed by the inverse rotation of every value row: with v
+ * the decoded f32 values of a row, values_out[c] =
+ * bf16( (H v)[c] * (1/16) * signs[c] ), H the 256-point Walsh-Hadamard
+ * matrix ((-1)^popcount(c & j)), computed by butterflies over the column
+ * bits 0..7 in that order (each a + b, a - b in f32, as the page's two
+ * radix-16 passes).  Requires head_dim 256, key_bits 8, value_bits 3, both
+ * groups 32 and value_out_bf16 = 1 (the pages' regime; any scale dtype is
+ * taken).  signs: f32 [256]. */
+trellis_status trellis_kv_decode_inverse256(const uint8_t* key_codes, const void* key_scales, const void* key_zeros,
+                                            const uint8_t* value_codes, const void* value_scales,
+                                            const float* centroids, const float* signs,
+                                            const trellis_kv_geometry* g, void* keys_out, void* values_out,
+                                            void* stream);
+
+/*
  * Measurement aid: `iters` rounds of 8 random 4-byte gathers per thread from
  * a 4096-entry f32 table held in shared memory, on `blocks` CTAs of 1024
  * threads; one float per thread goes to sink (f32 [blocks*1024]) so nothing

@@ -194,6 +194,33 @@ def test_gate_up_prefill_validation(lib):
     assert f(_p(A), 8, _p(A), _p(A), _p(A), _p(A), _p(A), ctypes.byref(gu), _p(A), None) == GEOM
 
 
+def test_kv_decode_validation(lib):
+    from trellis_coded_quantized_gb300 import kv_geometry
+    f, fi = lib.trellis_kv_decode, lib.trellis_kv_decode_inverse256
+    g = kv_geometry(8, 256, 8, 3)
+    args = [_p(A)] * 6
+    assert f(None, *args[1:], ctypes.byref(g), _p(A), _p(A), None) == NULL
+    assert f(*args, None, _p(A), _p(A), None) == NULL
+    assert fi(*args, None, ctypes.byref(g), _p(A), _p(A), None) == NULL
+    for field, value in (("rows", 0), ("head_dim", 96), ("key_bits", 3), ("value_bits", 6), ("key_group", 16),
+                         ("value_group", 128), ("key_scale_dtype", 3), ("value_out_bf16", 2)):
+        bad = kv_geometry(8, 256, 8, 3)
+        setattr(bad, field, value)
+        assert f(*args, ctypes.byref(bad), _p(A), _p(A), None) == GEOM, field
+    assert f(_p(U), *args[1:], ctypes.byref(g), _p(A), _p(A), None) == ALIGN
+    assert f(*args, ctypes.byref(g), _p(A), _p(U), None) == ALIGN
+    odd = [_p(A), _p(A + 1)] + args[2:]                       # f16 scales at an odd address
+    assert f(*odd, ctypes.byref(g), _p(A), _p(A), None) == ALIGN
+    # the inverse takes only the pages' regime, with bf16 values
+    assert fi(*args, _p(A), ctypes.byref(g), _p(A), _p(A), None) == GEOM
+    for field, value in (("head_dim", 128), ("key_bits", 4), ("value_bits", 2), ("key_group", 64)):
+        bad = kv_geometry(8, 256, 8, 3, value_out_bf16=True)
+        setattr(bad, field, value)
+        assert fi(*args, _p(A), ctypes.byref(bad), _p(A), _p(A), None) == GEOM, field
+    gb = kv_geometry(8, 256, 8, 3, value_out_bf16=True)
+    assert fi(*args, _p(A + 2), ctypes.byref(gb), _p(A), _p(A), None) == ALIGN
+
+
 def test_product_path_never_uses_the_oracle():
     """The package and its CUDA sources neither import, include, link nor call
     the oracle (it is test infrastructure only)."""

@@ -156,6 +156,72 @@ def trellis_gate_up_prefill(x, gate_codes, gate_scales, up_codes, up_scales, lut
     return out
 
 
+DT_F32, DT_F16, DT_BF16 = 0, 1, 2      # trellis_dtype
+
+
+def kv_geometry(rows: int, head_dim: int, key_bits: int, value_bits: int, key_group: int = 32,
+                value_group: int = 32, key_scale_dtype: int = DT_F16, key_zero_dtype: int = DT_F16,
+                value_scale_dtype: int = DT_F16, value_out_bf16: bool = False) -> _lib.KvGeometry:
+    """Shape of a packed TurboQuant K/V cache of `rows` positions (B*H*N)."""
+    return _lib.KvGeometry(rows, head_dim, key_bits, value_bits, key_group, value_group, key_scale_dtype,
+                           key_zero_dtype, value_scale_dtype, 1 if value_out_bf16 else 0)
+
+
+def _scale_types(dt):
+    torch = _torch()
+    return (torch.float32,) if dt == DT_F32 else (torch.float16,) if dt == DT_F16 else _bf16_types()
+
+
+def _kv_inputs(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g):
+    torch = _torch()
+    u8 = (torch.uint8, torch.int8)
+    D = g.head_dim
+    return (_dev(key_codes, "key_codes", u8, (g.rows, D * g.key_bits // 8)),
+            _dev(key_scales, "key_scales", _scale_types(g.key_scale_dtype), (g.rows, D // g.key_group)),
+            _dev(key_zeros, "key_zeros", _scale_types(g.key_zero_dtype), (g.rows, D // g.key_group)),
+            _dev(value_codes, "value_codes", u8, (g.rows, D * g.value_bits // 8)),
+            _dev(value_scales, "value_scales", _scale_types(g.value_scale_dtype), (g.rows, D // g.value_group)),
+            _dev(centroids, "centroids", (torch.float32,), (1 << g.value_bits,)))
+
+
+def _kv_outputs(keys_out, values_out, g, like):
+    torch = _torch()
+    shape = (g.rows, g.head_dim)
+    if keys_out is None:
+        keys_out = torch.empty(shape, dtype=torch.bfloat16, device=like.device)
+    if values_out is None:
+        values_out = torch.empty(shape, dtype=torch.bfloat16 if g.value_out_bf16 else torch.float32,
+                                 device=like.device)
+    vt = _bf16_types() if g.value_out_bf16 else (torch.float32,)
+    return keys_out, values_out, _dev(keys_out, "keys_out", _bf16_types(), shape), _dev(values_out, "values_out",
+                                                                                         vt, shape)
+
+
+def trellis_kv_decode(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g,
+                      keys_out=None, values_out=None, stream=None):
+    """TurboQuant joint K/V decode: packed [rows, D*bits/8] uint8 codes,
+    per-group scales/zeros, f32 centroids -> (bf16 keys [rows, D], f32 or
+    bf16 values [rows, D])."""
+    ins = _kv_inputs(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g)
+    keys_out, values_out, kp, vp = _kv_outputs(keys_out, values_out, g, key_codes)
+    _check(_lib.load().trellis_kv_decode(*ins, ctypes.byref(g), kp, vp, _stream(stream)), "trellis_kv_decode")
+    return keys_out, values_out
+
+
+def trellis_kv_decode_inverse256(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, signs, g,
+                                 keys_out=None, values_out=None, stream=None):
+    """The decode at D = 256, 8-bit keys, 3-bit values, groups of 32, with
+    the inverse Walsh-Hadamard rotation of the values (x 1/16, x signs):
+    (bf16 keys, bf16 values)."""
+    torch = _torch()
+    ins = _kv_inputs(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g)
+    sp = _dev(signs, "signs", (torch.float32,), (256,))
+    keys_out, values_out, kp, vp = _kv_outputs(keys_out, values_out, g, key_codes)
+    _check(_lib.load().trellis_kv_decode_inverse256(*ins, sp, ctypes.byref(g), kp, vp, _stream(stream)),
+           "trellis_kv_decode_inverse256")
+    return keys_out, values_out
+
+
 def trellis_scatter_workspace_bytes(g, M: int, splits: int = 0) -> int:
     return int(_lib.load().trellis_scatter_workspace_bytes(ctypes.byref(g), M, splits))
 

@@ -14,7 +14,8 @@ EXPORTS = (
     "trellis_matvec", "trellis_gate_up_matvec", "trellis_prefill", "trellis_gate_up_prefill", "trellis_scatter", "trellis_scatter_f32",
     "trellis_round_bf16", "trellis_scatter_noalloc",
     "trellis_scatter_workspace_bytes",
-    "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_gather_probe",
+    "trellis_expand", "trellis_rmsnorm", "trellis_silu_mul", "trellis_kv_decode", "trellis_kv_decode_inverse256",
+    "trellis_gather_probe",
     "trellis_device_status", "trellis_strerror",
 )
 
@@ -30,6 +31,13 @@ class Geometry(ctypes.Structure):
                 ("interleave", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
+class KvGeometry(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("head_dim", ctypes.c_int32), ("key_bits", ctypes.c_int32),
+                ("value_bits", ctypes.c_int32), ("key_group", ctypes.c_int32), ("value_group", ctypes.c_int32),
+                ("key_scale_dtype", ctypes.c_int32), ("key_zero_dtype", ctypes.c_int32),
+                ("value_scale_dtype", ctypes.c_int32), ("value_out_bf16", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -38,6 +46,7 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     """Declare the C signatures of the entry points on a loaded library."""
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     G = ctypes.POINTER(Geometry)
+    KG = ctypes.POINTER(KvGeometry)
     sig = {
         "trellis_matvec": ([P, P, P, P, G, P, P], I32),
         "trellis_gate_up_matvec": ([P, P, P, P, P, P, G, P, P], I32),
@@ -51,6 +60,8 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         "trellis_expand": ([P, P, P, G, P, P, P], I32),
         "trellis_rmsnorm": ([P, I64, I64, ctypes.c_float, P, P], I32),
         "trellis_silu_mul": ([P, P, I64, P, P], I32),
+        "trellis_kv_decode": ([P, P, P, P, P, P, KG, P, P, P], I32),
+        "trellis_kv_decode_inverse256": ([P, P, P, P, P, P, P, KG, P, P, P], I32),
         "trellis_gather_probe": ([P, I32, I32, I32, P, P], I32),
         "trellis_device_status": ([ctypes.POINTER(I32)], I32),
         "trellis_strerror": ([I32], ctypes.c_char_p),

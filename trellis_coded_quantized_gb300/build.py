@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libtrellis.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["abi.cu", "expand.cu", "matvec.cu", "scatter.cu", "scatter_tc.cu", "prefill.cu", "glue.cu"]
+SOURCES = ["abi.cu", "expand.cu", "matvec.cu", "scatter.cu", "scatter_tc.cu", "prefill.cu", "glue.cu",
+           "turboquant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", INCLUDE, "-I", CSRC]

@@ -5,6 +5,7 @@
 #include "internal.h"
 
 #include <climits>
+#include <initializer_list>
 #include <mutex>
 
 namespace {
@@ -101,6 +102,36 @@ trellis_status scatter_common(const void* x, int32_t M, const uint32_t* codes, c
                                         static_cast<cudaStream_t>(stream)));
 }
 
+bool one_of(int v, std::initializer_list<int> set) {
+    for (int x : set)
+        if (v == x) return true;
+    return false;
+}
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t dt_size(int dt) { return dt == tcq::kDtF32 ? 4 : 2; }
+
+trellis_status check_kv(const uint8_t* kp, const void* ks, const void* kz, const uint8_t* vp, const void* vs,
+                        const float* centroids, const trellis_kv_geometry* g, void* k_out, void* v_out) {
+    if (!kp || !ks || !kz || !vp || !vs || !centroids || !g || !k_out || !v_out) return TRELLIS_ERR_NULL;
+    if (g->rows < 1 || !one_of(g->head_dim, {64, 128, 256, 512}) || !one_of(g->key_bits, {2, 4, 5, 8}) ||
+        !one_of(g->value_bits, {2, 3, 4, 5, 8}) || !one_of(g->key_group, {32, 64}) ||
+        !one_of(g->value_group, {32, 64}) || !one_of(g->key_scale_dtype, {0, 1, 2}) ||
+        !one_of(g->key_zero_dtype, {0, 1, 2}) || !one_of(g->value_scale_dtype, {0, 1, 2}) ||
+        !one_of(g->value_out_bf16, {0, 1}) || g->rows > ((int64_t)1 << 40) / g->head_dim)
+        return TRELLIS_ERR_GEOMETRY;
+    if (!aligned16(kp) || !aligned16(vp) || !aligned16(k_out) || !aligned16(v_out) || !aligned_to(centroids, 4) ||
+        !aligned_to(ks, dt_size(g->key_scale_dtype)) || !aligned_to(kz, dt_size(g->key_zero_dtype)) ||
+        !aligned_to(vs, dt_size(g->value_scale_dtype)))
+        return TRELLIS_ERR_ALIGN;
+    return TRELLIS_OK;
+}
+
+tcq::KvArgs kv_args(const uint8_t* kp, const void* ks, const void* kz, const uint8_t* vp, const void* vs,
+                    const float* centroids, const trellis_kv_geometry* g, void* k_out, void* v_out) {
+    return tcq::KvArgs{kp, ks, kz, vp, vs, centroids, g->rows, g->head_dim, g->key_bits, g->value_bits,
+                       g->key_group, g->value_group, g->key_scale_dtype, g->key_zero_dtype, g->value_scale_dtype,
+                       g->value_out_bf16, k_out, v_out};
+}
 }  // namespace
 
 extern "C" {
@@ -167,6 +198,39 @@ trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t*
                                                 static_cast<const uint16_t*>(up_scales),
                                                 static_cast<const uint16_t*>(x), M, static_cast<uint16_t*>(h_out),
                                                 d->status, d->sm_count, static_cast<cudaStream_t>(stream)));
+}
+
+trellis_status trellis_kv_decode(const uint8_t* key_codes, const void* key_scales, const void* key_zeros,
+                                 const uint8_t* value_codes, const void* value_scales, const float* centroids,
+                                 const trellis_kv_geometry* g, void* keys_out, void* values_out, void* stream) {
+    trellis_status st = check_kv(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g,
+                                 keys_out, values_out);
+    if (st != TRELLIS_OK) return st;
+    const DeviceFacts* d;
+    if ((st = current_device(&d)) != TRELLIS_OK) return st;
+    return launched(tcq::launch_kv_decode(kv_args(key_codes, key_scales, key_zeros, value_codes, value_scales,
+                                                  centroids, g, keys_out, values_out),
+                                          d->sm_count, static_cast<cudaStream_t>(stream)));
+}
+
+trellis_status trellis_kv_decode_inverse256(const uint8_t* key_codes, const void* key_scales, const void* key_zeros,
+                                            const uint8_t* value_codes, const void* value_scales,
+                                            const float* centroids, const float* signs,
+                                            const trellis_kv_geometry* g, void* keys_out, void* values_out,
+                                            void* stream) {
+    if (!signs) return TRELLIS_ERR_NULL;
+    trellis_status st = check_kv(key_codes, key_scales, key_zeros, value_codes, value_scales, centroids, g,
+                                 keys_out, values_out);
+    if (st != TRELLIS_OK) return st;
+    if (g->head_dim != 256 || g->key_bits != 8 || g->value_bits != 3 || g->key_group != 32 ||
+        g->value_group != 32 || g->value_out_bf16 != 1)
+        return TRELLIS_ERR_GEOMETRY;
+    if (!aligned_to(signs, 4)) return TRELLIS_ERR_ALIGN;
+    const DeviceFacts* d;
+    if ((st = current_device(&d)) != TRELLIS_OK) return st;
+    return launched(tcq::launch_kv_inverse256(kv_args(key_codes, key_scales, key_zeros, value_codes, value_scales,
+                                                      centroids, g, keys_out, values_out),
+                                              signs, d->sm_count, static_cast<cudaStream_t>(stream)));
 }
 
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {

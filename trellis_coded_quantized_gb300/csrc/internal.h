@@ -99,4 +99,26 @@ inline int scatter_splits(int64_t rows, int64_t cols, int M, int splits) {
 // Status codes a kernel may record in the device status word.
 constexpr int kStatusWaitTimeout = 1;
 
+// TurboQuant packed K/V decode (turboquant.cu).  Element types of the scale
+// and zero arrays (the values of trellis_dtype).
+constexpr int kDtF32 = 0, kDtF16 = 1, kDtBF16 = 2;
+struct KvArgs {
+    const uint8_t* kp;      // [rows, D*kbits/8]
+    const void* ks;         // [rows, D/kg]
+    const void* kz;         // [rows, D/kg]
+    const uint8_t* vp;      // [rows, D*vbits/8]
+    const void* vs;         // [rows, D/vg]
+    const float* centroids; // [1 << vbits]
+    int64_t rows;
+    int D, kbits, vbits, kg, vg;
+    int ks_dt, kz_dt, vs_dt;
+    int v_bf16;             // values out as bf16 (else f32)
+    void* k_out;            // bf16 [rows, D]
+    void* v_out;            // f32 or bf16 [rows, D]
+};
+cudaError_t launch_kv_decode(const KvArgs& a, int sm_count, cudaStream_t stream);
+// D = 256, kbits 8, vbits 3, groups of 32, bf16 values after the inverse
+// rotation with signs[256].
+cudaError_t launch_kv_inverse256(const KvArgs& a, const float* signs, int sm_count, cudaStream_t stream);
+
 }  // namespace tcq

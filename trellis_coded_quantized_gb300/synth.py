@@ -15,6 +15,7 @@ Recipes (all on bf16 carried as uint16 bit patterns):
   lut     f32:    N(0, 1) by Box-Muller on pairs of uniforms
   scales  bf16:   U[0.01, 0.03] rounded to bf16 (to nearest, ties to even)
   x       bf16:   N(0, 1) rounded to bf16
+  kv_cache: the TurboQuant K/V cache (recipe in its docstring)
 The bf16 rounding of drawn inputs uses PyTorch's CPU conversion, a library
 routine that neither the oracle nor the CUDA path uses.
 """
@@ -114,6 +115,48 @@ def problem(axis: int, m: int, rows: int, cols: int, k: int, seed: int = 0) -> d
         "scales": scales(seed, rows),
         "lut": lut(seed),
         "x": activations(seed, m, kin),
+    }
+
+
+# ----------------------------------------------------------------------------
+# TurboQuant packed K/V cache (the second workload)
+# ----------------------------------------------------------------------------
+
+TAG_KV_K, TAG_KV_V, TAG_KV_KS, TAG_KV_KZ, TAG_KV_VS, TAG_KV_C, TAG_KV_SIGN = 11, 12, 13, 14, 15, 16, 17
+
+
+def _bytes(seed: int, tag: int, n: int) -> np.ndarray:
+    return (stream_u64(seed, tag, n) >> np.uint64(56)).astype(np.uint8)
+
+
+def _as_dtype(v: np.ndarray, dtype: str) -> np.ndarray:
+    """f32 draws stored as f32, f16 (numpy's conversion) or bf16 bit patterns."""
+    if dtype == "f32":
+        return v.astype(np.float32)
+    if dtype == "f16":
+        return v.astype(np.float16)
+    return to_bf16_bits(v.astype(np.float32))
+
+
+def kv_cache(seed: int, rows: int, D: int, key_bits: int, value_bits: int, key_group: int = 32,
+             value_group: int = 32, dtypes=("f16", "f16", "f16")) -> dict:
+    """A packed K/V cache of `rows` positions: uniform code bytes; key scales
+    U[0.005, 0.05]; key zeros U[-2^(b-1) - 1, -2^(b-1) + 1] for b-bit
+    unsigned codes, U[-1, 1] for signed 8-bit ones; value scales
+    U[0.5, 1.5]; sorted N(0, 1) centroids (f32); signs +-1 (f32)."""
+    kdt, zdt, vdt = dtypes
+    gk, gv = D // key_group, D // value_group
+    kz_mid = 0.0 if key_bits == 8 else -float(1 << (key_bits - 1))
+    return {
+        "rows": rows, "D": D, "key_bits": key_bits, "value_bits": value_bits,
+        "key_group": key_group, "value_group": value_group, "dtypes": tuple(dtypes),
+        "kp": _bytes(seed, TAG_KV_K, rows * D * key_bits // 8).reshape(rows, -1),
+        "vp": _bytes(seed, TAG_KV_V, rows * D * value_bits // 8).reshape(rows, -1),
+        "ks": _as_dtype(0.005 + 0.045 * uniform(seed, TAG_KV_KS, rows * gk), kdt).reshape(rows, gk),
+        "kz": _as_dtype(kz_mid - 1.0 + 2.0 * uniform(seed, TAG_KV_KZ, rows * gk), zdt).reshape(rows, gk),
+        "vs": _as_dtype(0.5 + uniform(seed, TAG_KV_VS, rows * gv), vdt).reshape(rows, gv),
+        "centroids": np.sort(normal(seed, TAG_KV_C, 1 << value_bits)).astype(np.float32),
+        "signs": np.where(uniform(seed, TAG_KV_SIGN, D) < 0.5, -1.0, 1.0).astype(np.float32),
     }
 
 
