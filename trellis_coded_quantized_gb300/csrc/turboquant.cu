@@ -34,8 +34,8 @@ namespace tcq {
 namespace {
 
 constexpr int kTqThreads = 256;
-constexpr int kTqUnroll = 4;          // chunks per thread and iteration (joint decode)
-constexpr int kTqRowUnroll = 2;       // rows per warp and iteration (inverse)
+constexpr int kTqUnroll = 1;          // chunks per thread and iteration (joint decode)
+constexpr int kTqRowUnroll = 1;       // rows per warp and iteration (inverse)
 
 __device__ __forceinline__ float load_scalar(const void* p, int64_t i, int dtype) {
     if (dtype == kDtF32) return __ldg(static_cast<const float*>(p) + i);
@@ -83,7 +83,7 @@ __device__ __forceinline__ uint4 decode_keys8(uint64_t run, float zero, float sc
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(kTqThreads, 4)
+__global__ void __launch_bounds__(kTqThreads)
 kv_decode_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks, const void* __restrict__ kz,
                  const uint8_t* __restrict__ vp, const void* __restrict__ vs, const float* __restrict__ centroids,
                  int64_t rows, int D, int kg, int vg, int ks_dt, int kz_dt, int vs_dt, int v_bf16,
@@ -96,11 +96,13 @@ kv_decode_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks, co
     // previous kernel of the stream
     pdl_wait();
     __syncthreads();
-    const int cpr = D >> 3;           // 8-column chunks per row
+    const int cpr = D >> 3;           // 8-column chunks per row: 8 .. 64, a power of two
+    const int cshift = 31 - __clz(cpr);
     const int64_t total = rows * cpr;
-    const int kgr = D / kg, vgr = D / vg;
+    const int kgs = 31 - __clz(kg), vgs = 31 - __clz(vg);   // groups of 32 or 64
+    const int kgr = D >> kgs, vgr = D >> vgs;
     // kTqUnroll chunks per thread and iteration, all their loads issued
-    // before the first is used (more bytes in flight per SM)
+    // before the first is used
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total; t0 += kTqUnroll * stride) {
         uint64_t krun[kTqUnroll], vrun[kTqUnroll];
@@ -109,22 +111,22 @@ kv_decode_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks, co
         for (int u = 0; u < kTqUnroll; ++u) {
             const int64_t t = t0 + u * stride;
             if (t >= total) break;
-            const int64_t r = t / cpr;
-            const int c = (int)(t - r * cpr);
+            const int64_t r = t >> cshift;
+            const int c = (int)t & (cpr - 1);
             const int col = c << 3;
             krun[u] = load_run<KB>(kp + r * (int64_t)(D * KB / 8), (int64_t)c * KB);
             vrun[u] = load_run<VB>(vp + r * (int64_t)(D * VB / 8), (int64_t)c * VB);
-            const int64_t kgi = r * kgr + col / kg;
+            const int64_t kgi = r * kgr + (col >> kgs);
             kzv[u] = load_scalar(kz, kgi, kz_dt);
             ksv[u] = load_scalar(ks, kgi, ks_dt);
-            vsv[u] = load_scalar(vs, r * vgr + col / vg, vs_dt);
+            vsv[u] = load_scalar(vs, r * vgr + (col >> vgs), vs_dt);
         }
         #pragma unroll
         for (int u = 0; u < kTqUnroll; ++u) {
             const int64_t t = t0 + u * stride;
             if (t >= total) break;
-            const int64_t r = t / cpr;
-            const int col = (int)(t - r * cpr) << 3;
+            const int64_t r = t >> cshift;
+            const int col = ((int)t & (cpr - 1)) << 3;
             *reinterpret_cast<uint4*>(k_out + r * D + col) = decode_keys8<KB>(krun[u], kzv[u], ksv[u]);
             float v[8];
             #pragma unroll
@@ -144,18 +146,17 @@ kv_decode_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks, co
 }
 
 // One warp per row; D = 256, 8-bit keys, 3-bit values, groups of 32.
-__global__ void __launch_bounds__(kTqThreads, 4)
+__global__ void __launch_bounds__(kTqThreads, 6)
 kv_inverse256_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks, const void* __restrict__ kz,
                      const uint8_t* __restrict__ vp, const void* __restrict__ vs,
                      const float* __restrict__ centroids, const float* __restrict__ signs, int64_t rows,
                      int ks_dt, int kz_dt, int vs_dt, uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out) {
     __shared__ float cent[8];
+    __shared__ float sgn[256];
     pdl_release();
     const int lane = threadIdx.x & 31;
     if (threadIdx.x < 8) cent[threadIdx.x] = __ldg(centroids + threadIdx.x);
-    float sg[8];
-    #pragma unroll
-    for (int e = 0; e < 8; ++e) sg[e] = __ldg(signs + 8 * lane + e);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sgn[i] = __ldg(signs + i);
     pdl_wait();
     __syncthreads();
     const int col = 8 * lane;
@@ -209,23 +210,25 @@ kv_inverse256_kernel(const uint8_t* __restrict__ kp, const void* __restrict__ ks
             uint32_t w[4];
             #pragma unroll
             for (int p = 0; p < 4; ++p)
-                w[p] = pack_bf16x2(__fmul_rn(__fmul_rn(x[2 * p], 0.0625f), sg[2 * p]),
-                                   __fmul_rn(__fmul_rn(x[2 * p + 1], 0.0625f), sg[2 * p + 1]));
+                w[p] = pack_bf16x2(__fmul_rn(__fmul_rn(x[2 * p], 0.0625f), sgn[col + 2 * p]),
+                                   __fmul_rn(__fmul_rn(x[2 * p + 1], 0.0625f), sgn[col + 2 * p + 1]));
             *reinterpret_cast<uint4*>(v_out + r * 256 + col) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
 
-int tq_grid(int64_t work_items, int per_block, int sm_count) {
+// Enough CTAs for the work, at most one full wave (`per_sm` resident CTAs
+// per SM); the kernels loop over the rest.
+int tq_grid(int64_t work_items, int per_block, int sm_count, int per_sm) {
     int64_t g = (work_items + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 152) * 8;
+    const int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 152) * per_sm;
     if (g > cap) g = cap;
     return g < 1 ? 1 : (int)g;
 }
 
 template <int KB, int VB>
 cudaError_t launch_kv(const KvArgs& a, int sm_count, cudaStream_t stream) {
-    const int grid = tq_grid(a.rows * (a.D / 8), kTqThreads, sm_count);
+    const int grid = tq_grid(a.rows * (a.D / 8), kTqThreads, sm_count, 8);
     const cudaError_t e = launch_pdl(kv_decode_kernel<KB, VB>, dim3(grid), dim3(kTqThreads), 0, stream, a.kp, a.ks,
                                      a.kz, a.vp, a.vs, a.centroids, a.rows, a.D, a.kg, a.vg, a.ks_dt, a.kz_dt,
                                      a.vs_dt, a.v_bf16, static_cast<uint16_t*>(a.k_out), a.v_out);
@@ -258,7 +261,7 @@ cudaError_t launch_kv_decode(const KvArgs& a, int sm_count, cudaStream_t stream)
 }
 
 cudaError_t launch_kv_inverse256(const KvArgs& a, const float* signs, int sm_count, cudaStream_t stream) {
-    const int grid = tq_grid(a.rows, kTqThreads / 32, sm_count);
+    const int grid = tq_grid(a.rows, kTqThreads / 32, sm_count, 6);
     const cudaError_t e = launch_pdl(kv_inverse256_kernel, dim3(grid), dim3(kTqThreads), 0, stream, a.kp, a.ks, a.kz,
                                      a.vp, a.vs, a.centroids, signs, a.rows, a.ks_dt, a.kz_dt, a.vs_dt,
                                      static_cast<uint16_t*>(a.k_out), static_cast<uint16_t*>(a.v_out));
