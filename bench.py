@@ -407,7 +407,7 @@ def gather_floor_s(weights: float, rates: dict, sm: int, sm_mhz) -> float:
     return weights / (r["per_sm_per_clock"] * sm * mhz * 1e6)
 
 
-def kv_lines(torch, tcq, device, stream, hbm):
+def kv_lines(torch, tcq, device, stream, hbm, only=None, steps=50, warmup=3):
     """The TurboQuant packed K/V decode (the second workload): the pages'
     measured regime (D 256, 8-bit keys, 3-bit values, f16 scales, groups of
     32) at B1 H4 N65536, joint decode (f32 values) and the inverse-256
@@ -423,6 +423,8 @@ def kv_lines(torch, tcq, device, stream, hbm):
     for name, rows, D, kb, vb, inverse in (("kv_decode_D256_k8v3", 4 * 65536, 256, 8, 3, False),
                                            ("kv_inverse256_D256_k8v3", 4 * 65536, 256, 8, 3, True),
                                            ("kv_decode_D128_k4v4", 4 * 131072, 128, 4, 4, False)):
+        if only is not None and name != only:
+            continue
         c = synth.kv_cache(11, rows, D, kb, vb)
         g = tcq.kv_geometry(rows, D, kb, vb, value_out_bf16=inverse)
         args = [dev(c[n]) for n in ("kp", "ks", "kz", "vp", "vs", "centroids")]
@@ -433,8 +435,8 @@ def kv_lines(torch, tcq, device, stream, hbm):
             fn = lambda i: tcq.trellis_kv_decode_inverse256(*args, signs, g, ko, vo)
         else:
             fn = lambda i: tcq.trellis_kv_decode(*args, g, ko, vo)
-        tb, _ = time_launches(torch, fn, 50, 3, stream, lambda: None, per_launch=False)
-        tb = tb * 1e-3 / 50
+        tb, _ = time_launches(torch, fn, steps, warmup, stream, lambda: None, per_launch=False)
+        tb = tb * 1e-3 / steps
         nbytes = sum(a.numel() * a.element_size() for a in args) + ko.numel() * 2 + vo.numel() * vo.element_size()
         out[name] = {"us_back_to_back": round(tb * 1e6, 2), "rows": rows, "bytes": nbytes,
                      "gbs": round(nbytes / tb / 1e9, 1), "frac_of_hbm": round(nbytes / tb / 1e9 / hbm, 4)}
@@ -523,6 +525,27 @@ def secondary(torch, tcq, device, stream, peaks, l2, rates, sm, sm_mhz):
     torch.cuda.empty_cache()
     out.update(rates)
     return out
+
+
+def run_kv(args):
+    """The TurboQuant K/V decode alone (the second workload, for profiling
+    and for a stand-alone line): the pages' regime at B1 H4 N65536, W
+    warm-up and K timed launches back to back; one JSON line with the
+    achieved bandwidth against the measured HBM peak."""
+    import torch
+    import trellis_coded_quantized_gb300 as tcq
+    torch.cuda.set_device(0)
+    device = torch.device("cuda:0")
+    peaks, peak_src = measured_peaks()
+    name = "kv_inverse256_D256_k8v3" if args.workload == "kv-inverse" else "kv_decode_D256_k8v3"
+    rec = kv_lines(torch, tcq, device, torch.cuda.current_stream(), peaks["hbm_gbs"], only=name,
+                   steps=args.steps, warmup=args.warmup)[name]
+    print(json.dumps({"metric": "TurboQuant K/V decode GB/s (inputs read + outputs written once)",
+                      "value": rec["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "higher_is_better": True, "data": "synthetic", "config": {"workload": name, "rows": rec["rows"]},
+                      "roofline": {"bound": "hbm", "achieved": rec["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": rec["frac_of_hbm"], "peak_source": peak_src},
+                      "us_back_to_back": rec["us_back_to_back"], "status": tcq.trellis_device_status()}))
 
 
 def run_ours(args):
@@ -810,7 +833,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode-matvec", "tiny-matvec", "prefill", "scatter"],
+    ap.add_argument("--workload", choices=["decode-matvec", "tiny-matvec", "prefill", "scatter", "kv-decode",
+                                           "kv-inverse"],
                     default="decode-matvec")
     ap.add_argument("--M", type=int, default=0, help="activation rows (prefill: 32, scatter: 1)")
     ap.add_argument("--k", type=int, default=0, help="bits per symbol of the prefill (4)")
@@ -825,6 +849,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in ("kv-decode", "kv-inverse"):
+        run_kv(args)
     else:
         run_ours(args)
 

@@ -89,10 +89,12 @@ struct PfLayout {
     static constexpr int kXChunk = NPAD * 128;             // one 64-column K chunk
     static constexpr int kCodeOff = kPfAStages * kXStage;
     static constexpr int kCodeStage = kPfRows * kPitch;
-    static constexpr int kLutOff = kCodeOff + kPfCodeStages * kCodeStage;
-    static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
+    static constexpr int kBarOff = kCodeOff + kPfCodeStages * kCodeStage;
     static constexpr int kBytes = kBarOff + 128;
-    static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
+    // the codebook copies come first, at the start of the dynamic shared
+    // memory (a constant address the gathers fold into their offset); the
+    // region above starts at the next 1024-byte boundary
+    static constexpr int kAlloc = (int)kLutRepBytes + kBytes + 1024;
 };
 
 // Words of the kPfUnits units of one block quarter of one row from the
@@ -132,15 +134,15 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                int rows, int cols, int interleave, int tile_rows, uint16_t* __restrict__ out,
                int* __restrict__ status) {
     using Lay = PfLayout<K, NPAD>;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     pdl_release();
     // 1024-byte aligned base, derived by pointer arithmetic on the shared
     // array (an integer round trip would lose the shared address space and
     // turn every table gather into a generic load)
-    uint8_t* base = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
+    float* lut_s = reinterpret_cast<float*>(smem_raw);
+    uint8_t* base = smem_raw + kLutRepBytes + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* xs = base;
     uint8_t* cs = base + Lay::kCodeOff;
-    float* lut_s = reinterpret_cast<float*>(base + Lay::kLutOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);   // decoders + activations
     uint64_t* empty = full + kPfAStages;                                  // MMA done with a stage
     uint64_t* cfull = empty + kPfAStages;                                 // code tile landed
@@ -198,8 +200,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         const float s_g = valid ? bf16_bits_to_float(__ldg(scales + row0 + rl)) : 0.f;
         const float s_u = GU && valid ? bf16_bits_to_float(__ldg(scales_u + row0 + rl)) : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        // shared address of this lane's codebook copy (entry e at +32 e)
-        const uint32_t lut_sa = tc::smem_addr(lut_s) + lut_rep_lane_offset();
+        const uint32_t gofs = lut_rep_lane_offset();     // this lane's codebook copy
         for (int b = 0; b < nbt; ++b) {
             const float s = GU && b >= nblocks ? s_u : s_g;
             const int stage = b % kPfAStages, use = b / kPfAStages;
@@ -219,17 +220,13 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                 for (int j = 0; j <= K; ++j) w[j] = cw[uu * K + j];   // neighbour is the next unit's first word
                 uint32_t r[16];
                 if (valid) {                                // lanes past the CTA's rows issue no gathers
-                    // all 32 gathers of the unit are issued before the first
-                    // is used (one load-pipe round trip per unit, not several)
-                    uint32_t v[32];
+                    // the unit's 32 codebook values first, then the scaling
+                    float v[32];
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j])
-                                     : "r"(lut_sa + win_off_sh<K, kLutRepShift>(w, 31 - j)));
+                    for (int j = 0; j < 32; ++j) v[j] = lut_at(lut_s, win_off_sh<K, kLutRepShift>(w, 31 - j) | gofs);
                     #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        r[j] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * j]), s),
-                                           __fmul_rn(__uint_as_float(v[2 * j + 1]), s));
+                        r[j] = pack_bf16x2(__fmul_rn(v[2 * j], s), __fmul_rn(v[2 * j + 1], s));
                 } else {
                     #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = 0u;
