@@ -55,8 +55,11 @@ cudaError_t launch_scatter_tc(const Packed& p, const uint16_t* x, int M, int spl
 // Most CTAs of the tensor-core scatter (its fix-up space is sized for them;
 // GB300 has 152 SMs).
 constexpr int kScatterTcMaxCtas = 160;
-// Fewest activation rows that take the tensor-core scatter.
+// Fewest activation rows that take the tensor-core scatter, and the split
+// count from which the mma.sync kernel (one CTA per split) takes over from
+// the tcgen05 one.
 constexpr int kScatterTcMinRows = 3;
+constexpr int kScatterTcMaxSplits = 128;
 // Whether a scatter call takes the tensor-core path (and its fix-up space).
 inline bool scatter_uses_tc(int M, bool unrounded) { return !unrounded && M >= kScatterTcMinRows; }
 // Floats of fix-up space the scatter needs besides the partials.

@@ -546,8 +546,13 @@ constexpr int kMmaMinRows = TCQ_MMA_MIN_ROWS;
 cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits,
                            float* partial, float* fix, void* out, bool out_f32, int* status, int sm_count,
                            cudaStream_t stream) {
-    // 3 and more activation rows, rounded contract: the tcgen05 kernel
-    if (scatter_uses_tc(M, p.unrounded))
+    // 3 and more activation rows, rounded contract, fewer than 128 splits:
+    // the tcgen05 kernel, whose stream-K schedule fills every SM whatever the
+    // split count.  From 128 splits one mma.sync CTA per split fills the SMs
+    // as well and has no per-item overhead (17408 x 5120, k=3, back to back:
+    // M=4 at 128 splits 56.5 us against 70.9 on tcgen05; M=16 at 128 splits
+    // 79.3 against 86.1; M=16 at 8 splits 57.1 on tcgen05 against 893).
+    if (scatter_uses_tc(M, p.unrounded) && splits < kScatterTcMaxSplits)
         return launch_scatter_tc(p, x, M, splits, partial, fix, out, out_f32, status, sm_count, stream);
     cudaError_t e;
     // up to 2 activation rows: FMA kernel, each decoded weight feeding every

@@ -60,16 +60,23 @@ class PackedMLPStack:
 
     def splits_for(self, M: int) -> int:
         """Row splits of the down projection: the constructor's, else one per
-        SM for the FMA scatter (M <= 2), and for the tensor-core scatter the
-        fewest splits whose row ranges are whole 16-row MMA steps at the
-        SM-limited step count (17408 rows on 152 SMs: 136 splits of 128)."""
+        SM for the FMA scatter (M <= 2), and from M = 3 the split-K
+        launcher's count (the library's default from M = 5: the power of two
+        at or above floor(tilesK / (tilesM * tilesN)), clamped to [2, 32];
+        8 for 17408 x 5120), which keeps the call on the tcgen05 scatter and
+        its stream-K schedule (at 8 splits 52-57 us at M = 4..16, against
+        56-86 us at 128 or more)."""
         if self.splits:
             return self.splits
         if M <= 2:
             return self.sm_count
-        steps = -(-self.inter // 16)
-        per = -(-steps // self.sm_count)
-        return -(-self.inter // (16 * per))
+        tiles_m = -(-M // 32)
+        tiles_n = -(-self.hidden // 32)
+        ratio = max(1, (self.inter // 16) // (tiles_m * tiles_n))
+        p2 = 1
+        while p2 < ratio:
+            p2 <<= 1
+        return min(32, max(2, p2))
 
     @property
     def packed_bytes(self) -> int:
