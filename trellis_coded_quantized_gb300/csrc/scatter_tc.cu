@@ -21,9 +21,9 @@
 //     (lane 32q+g) and 64q + 8g + 2r + 1 (lane 32q+g+8).  The rows of D past
 //     lane 16 of a quarter are never read;
 //   - B (activations x[m][r0 .. r0+63]) is K-major with the 128-byte swizzle;
-//   - a loader warp fills a ring of 4 slots, each the bundle of one stage:
+//   - a loader warp fills a ring of 8 slots (7 at N = 32), each the bundle of one stage:
 //     its code words (64 rows of one block, 128 bytes each), its 64 row
-//     scales and B, all by TMA tensor copies on one mbarrier, up to 4 stages
+//     scales and B, all by TMA tensor copies on one mbarrier, up to 8 stages
 //     ahead.  The copies bypass the load/store pipe that the codebook
 //     gathers keep busy (per-thread cp.async copies there took microseconds
 //     to land).  Rows whose first index is not a multiple of 8 fall back to
@@ -64,7 +64,6 @@ constexpr int kStThreads = 25 * 32;
 constexpr int kStRows = 64;                     // rows (K) of a stage: 4 MMA steps of 16
 constexpr int kStSteps = kStRows / 16;
 constexpr int kStStages = 3;                    // stages of decoded weights (A, tensor memory)
-constexpr int kStCStages = 4;                   // stages of code tiles
 constexpr int kStPitch = 128;                   // bytes per row of a code tile
 constexpr int kStCBytes = kStRows * kStPitch;   // one code tile (8 KB)
 // Per code slot, written by the loader with the tile: the stage's 64 row
@@ -80,16 +79,22 @@ constexpr uint64_t kStWaitNs = 1000000000ull;
 
 template <int NPAD>
 struct StLayout {
+    // slots of the TMA ring (code tile, scales and activations of a stage):
+    // the loader refills a slot once the MMAs of its stage are done, and a
+    // stage's copies take microseconds from HBM, so the ring runs as deep as
+    // shared memory allows (8 slots against 4: 3% faster at M = 4..32)
+    static constexpr int kCStages = NPAD <= 16 ? 8 : 7;
     static constexpr int kB = NPAD * 128;       // activations of one stage: NPAD rows x 64 K
     static constexpr int kCOff = 0;             // code tiles: 1024-byte aligned for the swizzled TMA
-    static constexpr int kBOff = kCOff + kStCStages * kStCBytes;
+    static constexpr int kBOff = kCOff + kCStages * kStCBytes;
     // per code slot: the stage's 64 row scales (TMA destination: 128-byte
     // aligned, here 1024) and its 16-byte descriptor
-    static constexpr int kSclOff = kBOff + kStCStages * kB;
-    static constexpr int kInfoOff = kSclOff + kStCStages * kStSclBytes;
-    static constexpr int kLutOff = (kInfoOff + kStCStages * 16 + 1023) / 1024 * 1024;
+    static constexpr int kSclOff = kBOff + kCStages * kB;
+    static constexpr int kInfoOff = kSclOff + kCStages * kStSclBytes;
+    static constexpr int kLutOff = (kInfoOff + kCStages * 16 + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kLutOff + (int)kLutRepBytes;
-    // 34 mbarriers, the tensor-memory address and the abort flag
+    // the mbarriers (at most 2 x 3 + 2 x 8 + 5), the tensor-memory address
+    // and the abort flag
     static constexpr int kBarBytes = 320;
     static constexpr int kBytes = kBarOff + kBarBytes;
     static constexpr int kAlloc = kBytes + 1024;    // slack for 1024-byte alignment
@@ -174,6 +179,7 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                   const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap, int tma_x) {
     using Lay = StLayout<NPAD>;
     constexpr int kDBuf = st_dbufs(NPAD);
+    constexpr int kCS = Lay::kCStages;
     static_assert(kDBuf * 4 * NPAD <= (int)kStACol, "D buffers overlap the A stages");
     extern __shared__ uint8_t smem_raw[];
     pdl_release();
@@ -186,13 +192,13 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
     uint64_t* afull = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);
     uint64_t* aempty = afull + kStStages;
     uint64_t* cfull = aempty + kStStages;
-    uint64_t* sempty = cfull + kStCStages;
-    uint64_t* dfull = sempty + kStCStages;                                 // an item's D complete
+    uint64_t* sempty = cfull + kCS;
+    uint64_t* dfull = sempty + kCS;                                 // an item's D complete
     uint64_t* dempty = dfull + 2;                                          // epilogue done with D
     uint64_t* done = dempty + 2;                                           // every MMA complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    static_assert((2 * kStStages + 2 * kStCStages + 5) * 8 + 8 <= Lay::kBarBytes, "barrier area too small");
+    static_assert((2 * kStStages + 2 * kCS + 5) * 8 + 8 <= Lay::kBarBytes, "barrier area too small");
     // every TMA destination: tiles 1024-byte aligned (128-byte swizzle), the
     // scales 128-byte aligned
     static_assert(Lay::kCOff % 1024 == 0 && kStCBytes % 1024 == 0 && Lay::kBOff % 1024 == 0 && Lay::kB % 1024 == 0,
@@ -211,7 +217,7 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             tc::mbar_init(&afull[i], kStDecWarps * 32);
             tc::mbar_init(&aempty[i], 4);
         }
-        for (int i = 0; i < kStCStages; ++i) {
+        for (int i = 0; i < kCS; ++i) {
             tc::mbar_init(&cfull[i], 1);
             tc::mbar_init(&sempty[i], 4);
         }
@@ -305,8 +311,8 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
             const bool more = h0.more != 0;
             // the next stage's slot, read while this stage is decoded
             if (more) {
-                const int cn = (j + 1) % kStCStages;
-                if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[cn], ((j + 1) / kStCStages) & 1, abort_flag, kStWaitNs)))
+                const int cn = (j + 1) % kCS;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&cfull[cn], ((j + 1) / kCS) & 1, abort_flag, kStWaitNs)))
                     break;
                 take_slot(cn, h1);
             }
@@ -381,15 +387,15 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
         // words past its row arrive as zeros), its 64 row scales, and the
         // activation tile x[0 .. NPAD)[r_begin .. +64) (K-major, 128-byte
         // swizzle; rows past M and past the matrix as zeros, rows past the
-        // split meet zero weights).  Slot j % 4 was last used by stage j - 4.
+        // split meet zero weights).  Slot j % kCS was last used by stage j - kCS.
         const uint64_t tmap_ptr = reinterpret_cast<uint64_t>(&tmap);
         if (lane == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(tmap_ptr) : "memory");
         Cursor cur;
         cursor_init(sc, cur, xb, xe);
         Stage st;
         for (int j = 0; next_stage(sc, cur, st); ++j) {
-            const int cs = j % kStCStages;
-            if (j >= kStCStages && !tc::warp_wait(&sempty[cs], ((j / kStCStages) - 1) & 1, abort_flag, kStWaitNs)) break;
+            const int cs = j % kCS;
+            if (j >= kCS && !tc::warp_wait(&sempty[cs], ((j / kCS) - 1) & 1, abort_flag, kStWaitNs)) break;
             const uint32_t bar = tc::smem_addr(&cfull[cs]);
             const uint32_t bs = b_base + (uint32_t)cs * Lay::kB;
             if (!tma_x) {
@@ -475,7 +481,7 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                         !tc::mbar_wait(&dempty[ic % kDBuf], ((ic / kDBuf) - 1) & 1, abort_flag, kStWaitNs))
                         break;
                 }
-                const int as = j % kStStages, cs = j % kStCStages;
+                const int as = j % kStStages, cs = j % kCS;
                 if (!tc::mbar_wait(&afull[as], (j / kStStages) & 1, abort_flag, kStWaitNs)) break;
                 tc::tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)((ic % kDBuf) * (4 * NPAD) + r * NPAD);
