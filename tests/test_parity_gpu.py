@@ -218,16 +218,18 @@ def test_scatter_partials(orc):
         assert np.all(np.abs(part[:, s, :] - ref[:, s, :]) <= 1e-5 * asum + 1e-30), s
 
 
+@pytest.mark.parametrize("splits", [8, 128])
 @pytest.mark.parametrize("M,k", [(16, 3), (5, 2), (32, 4), (3, 3), (4, 4)])
-def test_scatter_tensor_path_full_size(orc, M, k):
-    """3 or more activation rows take the tensor-core scatter (one pass)."""
+def test_scatter_tensor_path_full_size(orc, M, k, splits):
+    """3 or more activation rows take a tensor-core scatter in one pass:
+    tcgen05 below 128 splits, mma.sync from 128."""
     rows, cols = 17408, 5120
     p = synth.problem(0, M, rows, cols, k, seed=19)
     d = on_device(p)
-    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128))
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=splits))
     if M == 16:
-        _, y, a, _ = _oracle_axis0(orc, p)
-        check_close(orc, out, y, a, f"scatter tensor path M={M}")
+        _, y, a, _ = _oracle_axis0(orc, p, splits)
+        check_close(orc, out, y, a, f"scatter tensor path M={M} S={splits}")
     else:
         rng = np.random.default_rng(M)
         ms, js = rng.integers(0, M, 3000), rng.integers(0, cols, 3000)
@@ -280,13 +282,14 @@ def test_expand_interleave2_bit_exact(orc, axis, rows, cols, k):
     assert np.array_equal(host_bf16(win), owin) and np.array_equal(host_bf16(w), ow)
 
 
+@pytest.mark.parametrize("splits", [8, 128])
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_scatter_interleave2_full_size(orc, M):
+def test_scatter_interleave2_full_size(orc, M, splits):
     """The pages' k=3 axis-0 production layout at the full scatter geometry."""
     rows, cols, k = 17408, 5120, 3
     p = _inter(synth.problem(0, M, rows, cols, k, seed=15))
     d = on_device(p)
-    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128))
+    out = host_bf16(tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=splits))
     W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"], interleave=2)
     y, a, _, _ = orc.matmul_axis0(p["x"], W)
     check_close(orc, out, y, a, f"scatter interleave 2 M={M}")
