@@ -361,6 +361,11 @@ def time_launches(torch, fn, steps, warmup, stream, barrier, per_launch=True):
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    # Hold the stream for ~0.2 ms before the start event, so that the host
+    # has enqueued the first launches by the time it fires: otherwise the
+    # host's latency to enqueue the first step would be timed as GPU idle.
+    # The spin runs before the start event, outside the timed region.
+    torch.cuda._sleep(400_000)
     t0.record(stream)
     for i in range(steps):
         if per_launch:
