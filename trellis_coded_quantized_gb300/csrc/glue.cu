@@ -6,7 +6,56 @@
 namespace tcq {
 namespace {
 
-// One CTA per activation row: fp32 sum of squares, then x * rsqrt(mean + eps).
+// One CTA per activation row, the row held in registers: 16-byte loads of 8
+// values, fp32 sum of squares, then x * rsqrt(mean + eps) and 16-byte
+// stores -- one pass over memory (rows of 8 * 256 * kRmsChunks values at
+// most; x and out 16-byte aligned, D a multiple of 8).
+constexpr int kRmsChunks = 4;
+__global__ void __launch_bounds__(256)
+rmsnorm_vec_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* __restrict__ out) {
+    __shared__ float part[8];
+    pdl_wait();
+    pdl_release();
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)blockIdx.x * D);
+    uint4* orow = reinterpret_cast<uint4*>(out + (int64_t)blockIdx.x * D);
+    const int nc = (int)(D >> 3);
+    uint4 v[kRmsChunks];
+    float ss = 0.f;
+    #pragma unroll
+    for (int i = 0; i < kRmsChunks; ++i) {
+        const int c = threadIdx.x + 256 * i;
+        v[i] = c < nc ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_bits_to_float(w[q] & 0xffffu), hi = bf16_bits_to_float(w[q] >> 16);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+    #pragma unroll
+    for (int i = 0; i < kRmsChunks; ++i) {
+        const int c = threadIdx.x + 256 * i;
+        if (c >= nc) continue;
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t o[4];
+        #pragma unroll
+        for (int q = 0; q < 4; ++q)
+            o[q] = pack_bf16x2(bf16_bits_to_float(w[q] & 0xffffu) * inv, bf16_bits_to_float(w[q] >> 16) * inv);
+        orow[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// One CTA per activation row: fp32 sum of squares, then x * rsqrt(mean + eps)
+// (any D and alignment; two passes over the row).
 __global__ void __launch_bounds__(256)
 rmsnorm_kernel(const uint16_t* __restrict__ x, int64_t D, float eps, uint16_t* __restrict__ out) {
     __shared__ float part[8];
@@ -87,7 +136,10 @@ gather_probe_kernel(const float* __restrict__ lut, int iters, float* __restrict_
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t M, int64_t D, float eps,
                            uint16_t* out, cudaStream_t stream) {
-    const cudaError_t e = launch_pdl(rmsnorm_kernel, dim3((unsigned)M), dim3(256), 0, stream, x, D, eps, out);
+    const bool vec = D % 8 == 0 && D <= (int64_t)8 * 256 * kRmsChunks &&
+                     (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    const cudaError_t e = vec ? launch_pdl(rmsnorm_vec_kernel, dim3((unsigned)M), dim3(256), 0, stream, x, D, eps, out)
+                              : launch_pdl(rmsnorm_kernel, dim3((unsigned)M), dim3(256), 0, stream, x, D, eps, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

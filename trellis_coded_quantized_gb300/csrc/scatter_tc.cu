@@ -587,11 +587,14 @@ tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fi
             *pp = p;
         } else {
             const int64_t x0 = (int64_t)sc.NB * sc.prefix(s) + (int64_t)b * n;
-            const int g1 = sc.cta_of(x0), g2 = sc.cta_of(x0 + n - 1);
+            const bool sm32 = sc.small();
+            const int g1 = sm32 ? sc.cta_of32((uint32_t)x0) : sc.cta_of(x0);
+            const int g2 = sm32 ? sc.cta_of32((uint32_t)(x0 + n - 1)) : sc.cta_of(x0 + n - 1);
             p = *pp;
             if (g2 > g1) {
                 for (int g = g1 + 1; g <= g2; ++g) {
-                    if (sc.start(g) == sc.start(g + 1)) continue;     // a CTA with no steps
+                    const bool empty = sm32 ? sc.start32(g) == sc.start32(g + 1) : sc.start(g) == sc.start(g + 1);
+                    if (empty) continue;                                // a CTA with no steps
                     const float4 v = *reinterpret_cast<const float4*>(fix + ((int64_t)g * M + m) * kBT + cl);
                     p.x += v.x; p.y += v.y; p.z += v.z; p.w += v.w;
                 }

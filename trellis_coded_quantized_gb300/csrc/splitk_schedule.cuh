@@ -61,6 +61,14 @@ struct SplitSchedule {
     __host__ __device__ int64_t start(int g) const { return (int64_t)g * T / G; }
     // the CTA whose run holds step x (the last g with start(g) <= x)
     __host__ __device__ int cta_of(int64_t x) const { return (int)(((x + 1) * G - 1) / T); }
+    // The same two in 32-bit arithmetic, exact when T * G < 2^32 (any
+    // schedule below 26 million steps at 160 CTAs): a 64-bit division costs
+    // tens of dependent instructions.
+    __host__ __device__ bool small() const { return (uint64_t)T * (uint64_t)G < (1ull << 32); }
+    __host__ __device__ uint32_t start32(int g) const { return (uint32_t)g * (uint32_t)T / (uint32_t)G; }
+    __host__ __device__ int cta_of32(uint32_t x) const {
+        return (int)(((x + 1u) * (uint32_t)G - 1u) / (uint32_t)T);
+    }
     // split s, block b and step k within the item of step x; n = steps of the item
     __host__ __device__ void locate(int64_t x, int& s, int& b, int& k, int& n) const {
         const int64_t full = (int64_t)NB * F * nf;
