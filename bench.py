@@ -553,6 +553,42 @@ def run_kv(args):
                       "us_back_to_back": rec["us_back_to_back"], "status": tcq.trellis_device_status()}))
 
 
+def run_mlp(args):
+    """The synthetic packed SwiGLU stack alone: `--layers` layers (40), M
+    activation rows (16), W warm-up passes and K timed passes back to back;
+    one JSON line in tokens/s with the pass time and its share of the gather
+    ceiling.  For a stand-alone line and for launch lists of one layer's
+    kernels (a few layers suffice)."""
+    import torch
+    import trellis_coded_quantized_gb300 as tcq
+    from trellis_coded_quantized_gb300 import synth
+    from trellis_coded_quantized_gb300.mlp import PackedMLPStack
+    torch.cuda.set_device(0)
+    device = torch.device("cuda:0")
+    stream = torch.cuda.current_stream()
+    M = args.M or 16
+    stack = PackedMLPStack(layers=args.layers, k=3, device=device, m_max=max(16, M))
+    x0 = torch.from_numpy(synth.activations(0, M, stack.hidden).view(np.int16)).to(device).view(torch.bfloat16)
+    with ClockSampler(0) as clk:
+        rates, sm = gather_rates(torch, tcq, device, stream, clk)
+        h0 = time.perf_counter()
+        total_ms, _ = time_launches(torch, lambda i: stack.forward(x0, check=False), args.steps, args.warmup,
+                                    stream, lambda: None, per_launch=False)
+        h1 = time.perf_counter()
+    clocks = clk.summary(h0, h1)
+    t = total_ms * 1e-3 / args.steps
+    weights = len(stack.layers) * 3 * stack.inter * stack.hidden
+    floor = gather_floor_s(weights, rates, sm, clocks["sm_mhz"])
+    print(json.dumps({"metric": "tokens/s through the packed MLP stack", "value": round(M / t, 1), "unit": "tokens/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                      "data": "synthetic", "dtype": "bf16",
+                      "config": {"workload": f"mlp stack: {args.layers} layers, hidden 5120, intermediate 17408, k=3",
+                                 "M": M, "layers": args.layers},
+                      "ms_per_pass": round(t * 1e3, 4), "launches_per_pass": stack.launches_per_pass(M),
+                      "gather_floor_ms": round(floor * 1e3, 4), "frac_of_gather_floor": round(floor / t, 4),
+                      "clocks": clocks, "status": tcq.trellis_device_status()}))
+
+
 def run_ours(args):
     import torch
     import trellis_coded_quantized_gb300 as tcq
@@ -839,11 +875,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["decode-matvec", "tiny-matvec", "prefill", "scatter", "kv-decode",
-                                           "kv-inverse"],
+                                           "kv-inverse", "mlp"],
                     default="decode-matvec")
     ap.add_argument("--M", type=int, default=0, help="activation rows (prefill: 32, scatter: 1)")
     ap.add_argument("--k", type=int, default=0, help="bits per symbol of the prefill (4)")
     ap.add_argument("--splits", type=int, default=0, help="row splits of the scatter (128)")
+    ap.add_argument("--layers", type=int, default=40, help="layers of the MLP stack (--workload mlp)")
     ap.add_argument("--unrounded", action="store_true",
                     help="the contract without the bf16 rounding of the weight (matvec, scatter)")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary configurations")
@@ -856,6 +893,8 @@ def main():
         run_reference(args)
     elif args.workload in ("kv-decode", "kv-inverse"):
         run_kv(args)
+    elif args.workload == "mlp":
+        run_mlp(args)
     else:
         run_ours(args)
 

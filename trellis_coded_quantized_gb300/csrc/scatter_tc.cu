@@ -561,23 +561,35 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
 // out[m][c] = bf16( sum_s P[m][s][c] ).  The CTA that holds an item's first
 // step has written its share of P to the workspace; when the item runs on
 // into later CTAs, their fix-up slots are added to it here in CTA order and
-// the sum is stored back; P of an empty split is zero.  A CTA covers 32 columns of one activation
-// row with 32 groups of 8 threads; group g takes a contiguous run of splits
-// in order, then the 32 runs are added in order.
+// the sum is stored back; P of an empty split is zero.  A CTA covers
+// 4 * (256 / groups) columns of one activation row with `groups` groups of
+// 256 / groups threads (groups: the power of two at or below min(S, 32),
+// at least 4 so that a CTA stays within one 256-column block; few threads
+// idle for want of a split); group g takes a contiguous run of splits in
+// order, then the runs are added in order.
+__host__ __device__ inline int tc_rd_groups(int S) {
+    int g = 4;
+    while (g * 2 <= S && g * 2 <= 32) g *= 2;
+    return g;
+}
+
 template <bool F32OUT>
 __global__ void __launch_bounds__(256)
 tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fix, SplitSchedule sc,
                        int M, int C, void* __restrict__ out_) {
-    __shared__ float4 red[32][8];
+    __shared__ float4 red[256];
     pdl_wait();
     pdl_release();
-    const int m = blockIdx.y;
-    const int col = (blockIdx.x * 8 + (threadIdx.x & 7)) * 4;
-    const int b = col >> 8, cl = col & 255;
-    const int grp = threadIdx.x >> 3;
     const int S = sc.S;
-    const int per = (S + 31) / 32;
+    const int groups = tc_rd_groups(S);
+    const int ct = 256 / groups;                    // float4 columns per CTA
+    const int m = blockIdx.y;
+    const int grp = threadIdx.x / ct, ci = threadIdx.x - grp * ct;
+    const int col = (blockIdx.x * ct + ci) * 4;
+    const int b = col >> 8, cl = col & 255;
+    const int per = (S + groups - 1) / groups;
     const int s0 = grp * per, s1 = min(S, s0 + per);
+    const bool sm32 = sc.small();
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = s0; s < s1; ++s) {
         float4* pp = reinterpret_cast<float4*>(partial + ((int64_t)m * S + s) * C + col);
@@ -587,7 +599,6 @@ tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fi
             *pp = p;
         } else {
             const int64_t x0 = (int64_t)sc.NB * sc.prefix(s) + (int64_t)b * n;
-            const bool sm32 = sc.small();
             const int g1 = sm32 ? sc.cta_of32((uint32_t)x0) : sc.cta_of(x0);
             const int g2 = sm32 ? sc.cta_of32((uint32_t)(x0 + n - 1)) : sc.cta_of(x0 + n - 1);
             p = *pp;
@@ -603,12 +614,12 @@ tc_split_reduce_kernel(float* __restrict__ partial, const float* __restrict__ fi
         }
         a.x += p.x; a.y += p.y; a.z += p.z; a.w += p.w;
     }
-    red[grp][threadIdx.x & 7] = a;
+    red[threadIdx.x] = a;
     __syncthreads();
     if (grp == 0) {
-        float4 t = red[0][threadIdx.x];
-        for (int g = 1; g < 32; ++g) {
-            const float4 v = red[g][threadIdx.x];
+        float4 t = red[ci];
+        for (int g = 1; g < groups; ++g) {
+            const float4 v = red[g * ct + ci];
             t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
         }
         if constexpr (F32OUT) {
@@ -751,9 +762,11 @@ cudaError_t launch_scatter_tc(const Packed& p, const uint16_t* x, int M, int spl
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = out_f32 ? launch_pdl(tc_split_reduce_kernel<true>, dim3((unsigned)(C / 32), (unsigned)M), dim3(256), 0,
+    // C is a multiple of 256 and a CTA covers 32..256 columns
+    const dim3 rgrid((unsigned)(C / (4 * (256 / tc_rd_groups(splits)))), (unsigned)M);
+    e = out_f32 ? launch_pdl(tc_split_reduce_kernel<true>, rgrid, dim3(256), 0,
                              stream, partial, static_cast<const float*>(fix), sc, M, (int)C, out)
-                : launch_pdl(tc_split_reduce_kernel<false>, dim3((unsigned)(C / 32), (unsigned)M), dim3(256), 0,
+                : launch_pdl(tc_split_reduce_kernel<false>, rgrid, dim3(256), 0,
                              stream, partial, static_cast<const float*>(fix), sc, M, (int)C, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
