@@ -164,7 +164,7 @@ scatter_kernel(const uint16_t* __restrict__ x, int m0, const uint32_t* __restric
 constexpr int kRdGroups = 32;
 constexpr int kRdCols = 32;
 
-template <bool F32OUT>
+template <bool F32OUT, int B>
 __global__ void __launch_bounds__(256)
 split_reduce_kernel(const float* __restrict__ partial, int splits, int C, void* __restrict__ out_) {
     __shared__ float4 red[kRdGroups][kRdCols / 4];
@@ -180,9 +180,16 @@ split_reduce_kernel(const float* __restrict__ partial, int splits, int C, void* 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* p = reinterpret_cast<const float4*>(partial + (int64_t)m * splits * C) + cq;
     const int64_t stride = C / 4;
-    for (int s = s0; s < s1; ++s) {
-        const float4 v = __ldg(p + (int64_t)s * stride);
-        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    // the run's loads issued B at a time (one L2 round trip for up to B
+    // splits), then added in split order
+    for (int s = s0; s < s1; s += B) {
+        float4 v[B];
+        #pragma unroll
+        for (int j = 0; j < B; ++j)
+            if (s + j < s1) v[j] = __ldg(p + (int64_t)(s + j) * stride);
+        #pragma unroll
+        for (int j = 0; j < B; ++j)
+            if (s + j < s1) { a.x += v[j].x; a.y += v[j].y; a.z += v[j].z; a.w += v[j].w; }
     }
     red[grp][threadIdx.x & 7] = a;
     __syncthreads();
@@ -572,10 +579,21 @@ cudaError_t launch_scatter(const Packed& p, const uint16_t* x, int M, int splits
     const int C = (int)p.cols;
     // programmatic dependent launch: the reduction's CTAs are placed while
     // the last scatter pass still runs and start reading when it completes
-    e = out_f32 ? launch_pdl(split_reduce_kernel<true>, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0,
-                             stream, static_cast<const float*>(partial), splits, C, out)
-                : launch_pdl(split_reduce_kernel<false>, dim3((unsigned)(C / kRdCols), (unsigned)M), dim3(256), 0,
-                             stream, static_cast<const float*>(partial), splits, C, out);
+    // With at most two CTAs per SM (M = 1) each thread issues its run's
+    // loads 8 at a time; larger grids keep a split per load and 8 CTAs per
+    // SM in flight (the 8-wide form needs twice the registers).
+    const dim3 rgrid((unsigned)(C / kRdCols), (unsigned)M);
+    const bool wide = (int64_t)rgrid.x * rgrid.y <= 2 * (int64_t)sm_count;
+    if (out_f32)
+        e = wide ? launch_pdl(split_reduce_kernel<true, 8>, rgrid, dim3(256), 0, stream,
+                              static_cast<const float*>(partial), splits, C, out)
+                 : launch_pdl(split_reduce_kernel<true, 1>, rgrid, dim3(256), 0, stream,
+                              static_cast<const float*>(partial), splits, C, out);
+    else
+        e = wide ? launch_pdl(split_reduce_kernel<false, 8>, rgrid, dim3(256), 0, stream,
+                              static_cast<const float*>(partial), splits, C, out)
+                 : launch_pdl(split_reduce_kernel<false, 1>, rgrid, dim3(256), 0, stream,
+                              static_cast<const float*>(partial), splits, C, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
