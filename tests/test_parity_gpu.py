@@ -184,6 +184,7 @@ def test_scatter_full_size(orc, M):
     (300, 768, 2, 9, 1024), (513, 2048, 3, 4, 128), (129, 256, 4, 32, 64), (64, 5120, 3, 1, 128),
     (301, 512, 3, 7, 5), (301, 512, 4, 12, 13),         # odd rows and odd split sizes on the tensor path
     (2048, 512, 3, 32, 2), (4099, 256, 2, 9, 1),        # splits too long to stage their activations in shared memory
+    (1000, 768, 3, 4, 100),     # tensor path, 100 splits: reduction runs of 4 splits, the last runs empty
 ])
 def test_scatter_small(orc, rows, cols, k, M, splits):
     p = synth.problem(0, M, rows, cols, k, seed=7)
