@@ -37,7 +37,10 @@ def test_noalloc_matches_scatter_on_two_calls_in_a_row(orc):
         d = on_device(p)
         ref = tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128)
         out = torch.empty((M, cols), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        held = torch.cuda.memory_allocated()
         tcq.trellis_scatter_noalloc(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128, out=out)
+        assert torch.cuda.memory_allocated() == held, "the call with out given took memory from the allocator"
         torch.cuda.synchronize()
         got, want = host_bf16(out), host_bf16(ref)
         W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
