@@ -40,7 +40,8 @@ def test_noalloc_matches_scatter_on_two_calls_in_a_row(orc):
         torch.cuda.synchronize()
         held = torch.cuda.memory_allocated()
         tcq.trellis_scatter_noalloc(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128, out=out)
-        assert torch.cuda.memory_allocated() == held, "the call with out given took memory from the allocator"
+        # (the holdings may drop when Python frees a tensor of the previous round meanwhile)
+        assert torch.cuda.memory_allocated() <= held, "the call with out given took memory from the allocator"
         torch.cuda.synchronize()
         got, want = host_bf16(out), host_bf16(ref)
         W, _ = orc.expand(p["codes"], rows, cols, k, p["scales"], p["lut"])
