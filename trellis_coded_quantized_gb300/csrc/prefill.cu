@@ -17,8 +17,12 @@
 //     bytes more than a block, so 8 consecutive rows fall in 8 different
 //     bank groups; the decoders release a tile as soon as they hold its
 //     words, so the loads run up to 2 blocks ahead;
-//   - 1 activation-loader warp copies the activation tile of each block
-//     (cp.async, zero-filled rows M..N-1) into the swizzled layout;
+//   - 1 activation-loader thread copies the activation tile of each block
+//     with four TMA tensor copies (64 columns x N rows each, the 128-byte
+//     swizzle of the MMA's K-major B operand; rows M..N-1 lie outside the
+//     tensor and arrive as zeros), whose bytes complete the stage's "full"
+//     barrier together with the decoders' arrivals, so the activations need
+//     no load/store-pipe copies and no wait in the loader;
 //   - 16 decoder warps: warp w owns tensor-memory lane quarter w % 4 (32
 //     matrix rows, one row per thread) and quarter w / 4 of each block (2
 //     units of 32 columns).  A thread reads its row's words from the tile,
@@ -33,6 +37,10 @@
 //     block the accumulator is read back with tcgen05.ld by the lane-quarter
 //     warps and stored as bf16.
 // The K order of a block is the natural column order on both operands.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -72,6 +80,8 @@ __host__ __device__ constexpr uint32_t a_col(int st) { return st < 2 ? (uint32_t
 #define TCQ_WAIT_LIMIT_NS 1000000000ull
 #endif
 constexpr uint64_t kWaitLimitNs = TCQ_WAIT_LIMIT_NS;
+// After an abort: how long the activation loader waits for its last copies.
+constexpr uint64_t kDrainLimitNs = 2000000ull;
 
 #ifdef TCQ_TEST_HOOKS
 // test build only (see trellis_test_set_withhold at the end of this file)
@@ -132,7 +142,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                const uint16_t* __restrict__ scales, const uint32_t* __restrict__ codes_u,
                const uint16_t* __restrict__ scales_u, const float* __restrict__ lut,
                int rows, int cols, int interleave, int tile_rows, uint16_t* __restrict__ out,
-               int* __restrict__ status) {
+               int* __restrict__ status, const __grid_constant__ CUtensorMap xmap) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     pdl_release();
@@ -160,7 +170,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     pdl_wait();
     if (threadIdx.x == 0) {
         for (int st = 0; st < kPfAStages; ++st) {
-            tc::mbar_init(&full[st], kPfDecWarps * 32 + 32);
+            tc::mbar_init(&full[st], kPfDecWarps * 32 + 1);
             tc::mbar_init(&empty[st], 1);
         }
         for (int st = 0; st < kPfCodeStages; ++st) {
@@ -273,30 +283,39 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         }
     } else if (warp == kPfLoadWarp) {
         // ------------------------------------------------------------ activation loader
-        // 16-byte cp.async copies into the swizzled layout (rows >= M are
-        // zero-filled); the warp waits for its own copies, then fences them
-        // into the async proxy before arriving on full[stage].
-        const uint32_t xs_base = tc::smem_addr(xs);
-        for (int b = 0; b < nbt; ++b) {
-            const int stage = b % kPfAStages, use = b / kPfAStages;
-            if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
-            __syncwarp();
-            const int bb = GU && b >= nblocks ? b - nblocks : b;   // column block
-            const uint32_t st = xs_base + stage * Lay::kXStage;
-            #pragma unroll 8
-            for (int qd = lane; qd < NPAD * 32; qd += 32) {
-                const int n = qd >> 5, cc = qd & 31;
-                const int kc = cc >> 3, c = cc & 7;
-                const uint32_t dst = st + kc * Lay::kXChunk + n * 128 + ((c ^ (n & 7)) << 4);
-                const bool in = n < M;
-                const uint16_t* src = in ? x + (int64_t)n * cols + (int64_t)bb * kBT + cc * 8 : x;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-                             :: "r"(dst), "l"(src), "r"(in ? 16 : 0) : "memory");
+        // One thread: per block, four TMA tensor copies of 64 columns x NPAD
+        // rows into the stage; their bytes count towards full[stage].
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            const uint32_t xs_base = tc::smem_addr(xs);
+            int issued = 0;
+            for (int b = 0; b < nbt; ++b) {
+                const int stage = b % kPfAStages, use = b / kPfAStages;
+                if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+                const int bb = GU && b >= nblocks ? b - nblocks : b;   // column block
+                const uint32_t bar = tc::smem_addr(&full[stage]);
+                const uint32_t st = xs_base + stage * Lay::kXStage;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                             :: "r"(bar), "r"(Lay::kXStage) : "memory");
+                #pragma unroll
+                for (int kc = 0; kc < 4; ++kc)
+                    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3}], [%4];"
+                                 :: "r"(st + kc * Lay::kXChunk), "l"(reinterpret_cast<uint64_t>(&xmap)),
+                                    "r"(bb * kBT + kc * 64), "r"(0), "r"(bar) : "memory");
+                issued = b + 1;
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&full[stage]);
+            // no copy may still be in flight when the CTA ends: after an
+            // abort, wait for the last issued stages' barriers with a limit
+            // of its own (their phases may also lack the decoders' arrivals,
+            // so the limit, far longer than a copy takes, can run out)
+            if (*abort_flag) {
+                volatile int keep_waiting = 0;
+                for (int b = issued > kPfAStages ? issued - kPfAStages : 0; b < issued; ++b)
+                    tc::mbar_wait(&full[b % kPfAStages], (b / kPfAStages) & 1, &keep_waiting, kDrainLimitNs);
+            }
         }
+        __syncwarp();
     } else if (warp == kPfMmaWarp) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
@@ -362,6 +381,41 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
     if (threadIdx.x == 0 && *abort_flag) atomicOr(status, kStatusWaitTimeout);
 }
 
+// cuTensorMapEncodeTiled, found once through the runtime (no link-time
+// dependence on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn pf_encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// The activations x [M][cols] (bf16, 16-byte aligned, cols a multiple of
+// 256) with a box of 64 columns by npad rows and the 128-byte swizzle: one
+// K chunk of the MMA's B operand per copy; rows past M are filled with zeros.
+cudaError_t pf_x_tensor_map(const uint16_t* x, int M, int64_t cols, int npad, CUtensorMap* map) {
+    EncodeTiledFn enc = pf_encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)npad}, estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int K, int NPAD, bool GU>
 cudaError_t launch_kn(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x, int M,
                       uint16_t* out, int* status, int sm_count, cudaStream_t stream) {
@@ -375,8 +429,12 @@ cudaError_t launch_kn(const Packed& p, const uint32_t* codes_u, const uint16_t* 
     if (sm_count > 0 && p.rows > (int64_t)64 * sm_count && p.rows <= (int64_t)kPfRows * sm_count)
         tile_rows = (int)((p.rows + sm_count - 1) / sm_count);
     const unsigned grid = (unsigned)((p.rows + tile_rows - 1) / tile_rows);
+    alignas(64) CUtensorMap xmap;
+    e = pf_x_tensor_map(x, M, p.cols, NPAD, &xmap);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(prefill_kernel<K, NPAD, GU>, dim3(grid), dim3(kPfThreads), (size_t)smem, stream, x, M, p.codes,
-                   p.scales, codes_u, scales_u, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status);
+                   p.scales, codes_u, scales_u, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status,
+                   xmap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
