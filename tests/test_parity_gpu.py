@@ -353,9 +353,26 @@ def _ulps(a, b):
     return np.abs(fa - fb) / bf16_ulp(np.maximum(np.abs(fa), np.abs(fb)))
 
 
-def test_rmsnorm(orc):
-    x = synth.activations(11, 16, 5120)
+@pytest.mark.parametrize("M,D", [
+    (16, 5120),     # the MLP's rows: the one-pass kernel (rows held in registers)
+    (3, 8), (2, 8192),   # the one-pass kernel's smallest and largest rows
+    (5, 1001),      # D not a multiple of 8: the two-pass kernel
+    (2, 12288),     # longer than the one-pass kernel holds: the two-pass kernel
+])
+def test_rmsnorm(orc, M, D):
+    x = synth.activations(11, M, D)
     out = host_bf16(tcq.trellis_rmsnorm(dev(x), 1e-6))
+    assert np.all(_ulps(out, orc.rmsnorm(x, 1e-6)) <= 1.0)
+
+
+def test_rmsnorm_unaligned_rows_take_the_two_pass_kernel(orc):
+    import torch
+    M, D = 4, 5120
+    x = synth.activations(14, M, D)
+    buf = torch.empty(M * D + 1, dtype=torch.bfloat16, device="cuda")
+    xs = buf[1:].view(M, D)                         # 2-byte offset: not 16-byte aligned
+    xs.copy_(dev(x))
+    out = host_bf16(tcq.trellis_rmsnorm(xs, 1e-6))
     assert np.all(_ulps(out, orc.rmsnorm(x, 1e-6)) <= 1.0)
 
 
