@@ -11,12 +11,12 @@
 //     weights (rows of the matrix are MMA rows, "swap AB") held in TENSOR
 //     MEMORY, B = activations in shared memory (K-major, 128-byte swizzle),
 //     D = fp32 accumulator in tensor memory; N = 16 or 32 (M padded);
-//   - 1 code-loader warp: per 256-column block it copies the block of all
-//     128 rows in coalesced 16-byte cp.async chunks (completion tracked on
-//     an mbarrier) into one of 2 shared-memory tiles whose row pitch is 16
-//     bytes more than a block, so 8 consecutive rows fall in 8 different
-//     bank groups; the decoders release a tile as soon as they hold its
-//     words, so the loads run up to 2 blocks ahead;
+//   - 1 code-loader thread: per 256-column block one TMA tensor copy of
+//     the block of the CTA's rows (32 words per row with the 128-byte
+//     swizzle, so that 8 consecutive rows read 8 different 16-byte chunks)
+//     into one of 2 shared-memory tiles, completing on the tile's mbarrier;
+//     the decoders release a tile as soon as they hold its words, so the
+//     copies run up to 2 blocks ahead;
 //   - 1 activation-loader thread copies the activation tile of each block
 //     with four TMA tensor copies (64 columns x N rows each, the 128-byte
 //     swizzle of the MMA's K-major B operand; rows M..N-1 lie outside the
@@ -94,7 +94,10 @@ __device__ __forceinline__ bool test_withhold_arrival() {
 template <int K, int NPAD>
 struct PfLayout {
     static constexpr int kWpb = kBT * K / 32;              // words of one block
-    static constexpr int kPitch = kWpb * 4 + 16;           // bytes per row of a code tile
+    // bytes per row of a code tile: one 128-byte swizzle row (the TMA box
+    // is 32 words wide; past a block's kWpb words it holds the next block's
+    // first words, or zeros past the end of the matrix row)
+    static constexpr int kPitch = 128;
     static constexpr int kXStage = NPAD * kBT * 2;         // bytes of one activation stage
     static constexpr int kXChunk = NPAD * 128;             // one 64-column K chunk
     static constexpr int kCodeOff = kPfAStages * kXStage;
@@ -107,27 +110,34 @@ struct PfLayout {
     static constexpr int kAlloc = (int)kLutRepBytes + kBytes + 1024;
 };
 
-// Words of the kPfUnits units of one block quarter of one row from the
-// shared code tile, plus the neighbour word (first word of the next unit,
-// unit 0 for the last quarter).
+// Words of the kPfUnits units of one block quarter of row rl from the code
+// tile (128-byte rows with the 128-byte swizzle: 16-byte chunk c of row rl
+// sits at chunk c ^ (rl & 7)), plus the neighbour word (first word of the
+// next unit, unit 0 for the last quarter).  Eight consecutive rows read
+// eight different chunks, so a warp's vector loads take the fewest
+// wavefronts.
 template <int K>
-__device__ __forceinline__ void read_quarter(uint32_t* w, const uint8_t* row, int part) {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + part * kPfUnits * K;
+__device__ __forceinline__ uint32_t sw_word_off(int j, int rl) {
+    return (uint32_t)((((j >> 2) ^ (rl & 7)) << 4) | ((j & 3) << 2));
+}
+template <int K>
+__device__ __forceinline__ void read_quarter(uint32_t* w, const uint8_t* row, int rl, int part) {
+    const int j0 = part * kPfUnits * K;
     if constexpr (K == 3) {
         #pragma unroll
         for (int j = 0; j < kPfUnits * K; j += 2) {
-            const uint2 v = *reinterpret_cast<const uint2*>(p + j);
+            const uint2 v = *reinterpret_cast<const uint2*>(row + sw_word_off<K>(j0 + j, rl));
             w[j] = v.x; w[j + 1] = v.y;
         }
     } else {
         #pragma unroll
         for (int j = 0; j < kPfUnits * K; j += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p + j);
+            const uint4 v = *reinterpret_cast<const uint4*>(row + sw_word_off<K>(j0 + j, rl));
             w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
         }
     }
     const int nb = (part + 1 == kPfParts) ? 0 : (part + 1) * kPfUnits * K;
-    w[kPfUnits * K] = reinterpret_cast<const uint32_t*>(row)[nb];
+    w[kPfUnits * K] = *reinterpret_cast<const uint32_t*>(row + sw_word_off<K>(nb, rl));
 }
 
 // GU: the gate and up projections of a SwiGLU layer in one launch.  The CTA
@@ -142,7 +152,8 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
                const uint16_t* __restrict__ scales, const uint32_t* __restrict__ codes_u,
                const uint16_t* __restrict__ scales_u, const float* __restrict__ lut,
                int rows, int cols, int interleave, int tile_rows, uint16_t* __restrict__ out,
-               int* __restrict__ status, const __grid_constant__ CUtensorMap xmap) {
+               int* __restrict__ status, const __grid_constant__ CUtensorMap xmap,
+               const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap cmap_u) {
     using Lay = PfLayout<K, NPAD>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     pdl_release();
@@ -174,7 +185,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
             tc::mbar_init(&empty[st], 1);
         }
         for (int st = 0; st < kPfCodeStages; ++st) {
-            tc::mbar_init(&cfull[st], 32);
+            tc::mbar_init(&cfull[st], 1);
             tc::mbar_init(&cempty[st], kPfDecWarps * 32);
         }
         tc::mbar_init(done, 1);
@@ -217,7 +228,7 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
             const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
             if (!tc::mbar_wait(&cfull[cst], cuse & 1, abort_flag, kWaitLimitNs)) break;
             uint32_t cw[kPfUnits * K + 1];
-            read_quarter<K>(cw, cs + cst * Lay::kCodeStage + rl * Lay::kPitch, part);
+            read_quarter<K>(cw, cs + cst * Lay::kCodeStage + rl * Lay::kPitch, rl, part);
             tc::mbar_arrive(&cempty[cst]);                 // the code tile may be refilled
             if (b >= kPfAStages && !tc::mbar_wait(&empty[stage], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
             __syncwarp();
@@ -250,37 +261,51 @@ prefill_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restrict
         }
     } else if (warp == kPfCodeWarp) {
         // ------------------------------------------------------------ code loader
-        // The block of all valid rows in 16-byte cp.async chunks (a warp
-        // instruction covers 512 contiguous bytes of consecutive rows) into
-        // tile cst; each lane's copies arrive on cfull[cst] when they land.
-        // Up to kPfCodeStages blocks ahead of the decoders, which release a
-        // tile (cempty) as soon as they hold its words in registers.
-        const int64_t wpr = block_row_stride(nblocks, wpb, interleave);
-        constexpr int cpr = wpb / 4;                     // 16-byte chunks per row
-        const int nchunks = nvalid * cpr;
-        for (int b = 0; b < nbt; ++b) {
-            const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
-            if (b >= kPfCodeStages &&
-                !tc::mbar_wait(&cempty[cst], (cuse - 1) & 1, abort_flag, kWaitLimitNs)) break;
-            const uint32_t ct = tc::smem_addr(cs + cst * Lay::kCodeStage);
-            const bool upm = GU && b >= nblocks;
-            const uint32_t* src0 = (upm ? codes_u : codes) + (int64_t)row0 * wpr +
-                                   block_col_base(upm ? b - nblocks : b, rows, wpb, interleave);
-            for (int c = lane; c < nchunks; c += 32) {
-                const int r = c / cpr, part = c - (c / cpr) * cpr;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             :: "r"(ct + r * Lay::kPitch + part * 16), "l"(src0 + (int64_t)r * wpr + part * 4)
-                             : "memory");
-            }
+        // One thread: per block, one TMA tensor copy of the CTA's rows
+        // (32 words each, the 128-byte swizzle) into tile cst, completing on
+        // cfull[cst] with its bytes.  Up to kPfCodeStages blocks ahead of
+        // the decoders, which release a tile (cempty) as soon as they hold
+        // its words in registers.
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&cmap)) : "memory");
+            if (GU) asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&cmap_u)) : "memory");
+            const uint32_t tile_bytes = (uint32_t)tile_rows * Lay::kPitch;
+            int issued = 0;
+            for (int b = 0; b < nbt; ++b) {
+                const int cst = b % kPfCodeStages, cuse = b / kPfCodeStages;
+                if (b >= kPfCodeStages &&
+                    !tc::mbar_wait(&cempty[cst], (cuse - 1) & 1, abort_flag, kWaitLimitNs)) break;
 #ifdef TCQ_TEST_HOOKS
-            // test build only: with the hook set, lane 0 of CTA 0 withholds its
-            // arrival for the first code tile, so the decoders' bounded wait on
-            // it runs out and the kernel takes its abort path
-            if (b == 0 && lane == 0 && blockIdx.x == 0 && test_withhold_arrival()) continue;
+                // test build only: with the hook set, CTA 0 withholds its
+                // first code tile, so the decoders' bounded wait on it runs
+                // out and the kernel takes its abort path
+                if (b == 0 && blockIdx.x == 0 && test_withhold_arrival()) continue;
 #endif
-            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
-                         :: "r"(tc::smem_addr(&cfull[cst])) : "memory");
+                const bool upm = GU && b >= nblocks;
+                const int bb = upm ? b - nblocks : b;
+                const uint64_t map = reinterpret_cast<uint64_t>(upm ? &cmap_u : &cmap);
+                const uint32_t dst = tc::smem_addr(cs + cst * Lay::kCodeStage);
+                const uint32_t bar = tc::smem_addr(&cfull[cst]);
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(tile_bytes)
+                             : "memory");
+                if (interleave == 2)
+                    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                                 :: "r"(dst), "l"(map), "r"((bb & 1) * wpb), "r"(row0), "r"(bb >> 1), "r"(bar)
+                                 : "memory");
+                else
+                    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3}], [%4];"
+                                 :: "r"(dst), "l"(map), "r"(bb * wpb), "r"(row0), "r"(bar) : "memory");
+                issued = b + 1;
+            }
+            // no copy may still be in flight when the CTA ends: wait for the
+            // last issued tiles' bytes, with a limit of its own
+            volatile int keep_waiting = 0;
+            for (int b = issued > kPfCodeStages ? issued - kPfCodeStages : 0; b < issued; ++b)
+                tc::mbar_wait(&cfull[b % kPfCodeStages], (b / kPfCodeStages) & 1, &keep_waiting, kDrainLimitNs);
         }
+        __syncwarp();
     } else if (warp == kPfLoadWarp) {
         // ------------------------------------------------------------ activation loader
         // One thread: per block, four TMA tensor copies of 64 columns x NPAD
@@ -416,6 +441,37 @@ cudaError_t pf_x_tensor_map(const uint16_t* x, int M, int64_t cols, int npad, CU
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The codes as uint32 words with a box of 32 words (one 128-byte swizzle
+// row) by tile_rows rows: interleave 0 is [rows][nb * wpb], interleave 2 is
+// [nb / 2][rows][2 * wpb].  Past a block's wpb words the box reads the next
+// block's first words, or zeros past the end of the tensor's row.
+cudaError_t pf_code_tensor_map(const uint32_t* codes, int64_t rows, int64_t cols, int k, int interleave,
+                               int tile_rows, CUtensorMap* map) {
+    EncodeTiledFn enc = pf_encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t wpb = (cuuint64_t)(kBT * k / 32), nb = (cuuint64_t)(cols / kBT);
+    cuuint64_t dims[3], strides[2];
+    const cuuint32_t box[3] = {32, (cuuint32_t)tile_rows, 1}, estr[3] = {1, 1, 1};
+    cuuint32_t rank;
+    if (interleave == 2) {
+        rank = 3;
+        dims[0] = 2 * wpb;
+        dims[1] = (cuuint64_t)rows;
+        dims[2] = nb / 2;
+        strides[0] = dims[0] * 4;
+        strides[1] = strides[0] * dims[1];
+    } else {
+        rank = 2;
+        dims[0] = nb * wpb;
+        dims[1] = (cuuint64_t)rows;
+        strides[0] = dims[0] * 4;
+    }
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<uint32_t*>(codes), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int K, int NPAD, bool GU>
 cudaError_t launch_kn(const Packed& p, const uint32_t* codes_u, const uint16_t* scales_u, const uint16_t* x, int M,
                       uint16_t* out, int* status, int sm_count, cudaStream_t stream) {
@@ -429,12 +485,19 @@ cudaError_t launch_kn(const Packed& p, const uint32_t* codes_u, const uint16_t* 
     if (sm_count > 0 && p.rows > (int64_t)64 * sm_count && p.rows <= (int64_t)kPfRows * sm_count)
         tile_rows = (int)((p.rows + sm_count - 1) / sm_count);
     const unsigned grid = (unsigned)((p.rows + tile_rows - 1) / tile_rows);
-    alignas(64) CUtensorMap xmap;
+    alignas(64) CUtensorMap xmap, cmap, cmap_u;
     e = pf_x_tensor_map(x, M, p.cols, NPAD, &xmap);
     if (e != cudaSuccess) return e;
+    e = pf_code_tensor_map(p.codes, p.rows, p.cols, K, p.interleave, tile_rows, &cmap);
+    if (e != cudaSuccess) return e;
+    cmap_u = cmap;
+    if (GU) {
+        e = pf_code_tensor_map(codes_u, p.rows, p.cols, K, p.interleave, tile_rows, &cmap_u);
+        if (e != cudaSuccess) return e;
+    }
     e = launch_pdl(prefill_kernel<K, NPAD, GU>, dim3(grid), dim3(kPfThreads), (size_t)smem, stream, x, M, p.codes,
                    p.scales, codes_u, scales_u, p.lut, (int)p.rows, (int)p.cols, p.interleave, tile_rows, out, status,
-                   xmap);
+                   xmap, cmap, cmap_u);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
