@@ -307,6 +307,22 @@ def test_scatter_tensor_path_interleave2(orc, rows, cols, k, M, splits):
     check_close(orc, out, y, a, f"tensor scatter interleave 2 {rows}x{cols} k={k} M={M} S={splits}")
 
 
+@pytest.mark.parametrize("M,k", [(16, 3), (32, 2)])
+def test_prefill_interleave2_full_size(orc, M, k):
+    """Interleave 2 at 17408 x 5120: 115-row tiles, the code tiles copied as
+    3-d boxes (block pair, rows, words) that read past the block's words."""
+    rows, cols = 17408, 5120
+    p = _inter(synth.problem(1, M, rows, cols, k, seed=M + k))
+    d = on_device(p)
+    out = host_bf16(tcq.trellis_prefill(d["x"], d["codes"], d["scales"], d["lut"], d["g"]))
+    rng = np.random.default_rng(M * 3 + k)
+    ms = rng.integers(0, M, 3000)
+    js = rng.integers(0, rows, 3000)
+    y, a = orc.sample(p["x"], p["codes"], rows, cols, k, p["scales"], p["lut"], 1, ms, js, interleave=2)
+    check_close(orc, out[ms, js], y, a, f"prefill interleave 2 full M={M} k={k}")
+    assert tcq.trellis_device_status() == 0
+
+
 @pytest.mark.parametrize("k", [2, 3, 4])
 def test_axis1_interleave2(orc, k):
     rows, cols = 300, 1536
