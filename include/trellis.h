@@ -175,7 +175,11 @@ trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t*
  * axis in split order and rounds to bf16.
  *   x          bf16 [M, rows], 16-byte aligned
  *   splits     1..1024, or 0 for the default: 128 when M <= 4 (scatter.ts,
- *              SCATTER_SPLITS), else the split count of the split-K
+ *              SCATTER_SPLITS), and 128 at every M under
+ *              TRELLIS_FLAG_UNROUNDED (the contract of scatter.ts's
+ *              balanced scatter kernels, which run SCATTER_SPLITS ranges;
+ *              its kernel from 3 rows takes one CTA per split), else the
+ *              split count of the split-K
  *              launcher (splitk-prefill.ts): with tilesM = ceil(M/32),
  *              tilesN = ceil(cols/32), tilesK = floor(rows/16) and
  *              ratio = max(1, floor(tilesK / (tilesM*tilesN))), the power of

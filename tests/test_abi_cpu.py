@@ -123,7 +123,8 @@ def test_workspace_size(lib):
 
 def test_default_split_count(lib):
     """splits = 0: 128 up to 4 activation rows, else the split-K launcher's
-    rule (the hand-worked values of tests/golden/default_splits.txt)."""
+    rule (the hand-worked values of tests/golden/default_splits.txt); 128 at
+    every M under the unrounded contract."""
     import pins
     for rows, cols, M, want in pins.read_default_splits():
         g0 = geometry(0, rows, cols, 3)
@@ -132,6 +133,10 @@ def test_default_split_count(lib):
     g0 = geometry(0, 17408, 5120, 3)
     assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 4, 0) == 4 * 128 * 5120 * 4 + _fix(4)
     assert lib.trellis_scatter_workspace_bytes(ctypes.byref(g0), 8, 0) == 8 * 8 * 5120 * 4 + _fix(8)
+    # the unrounded contract keeps scatter.ts's 128 ranges at every M
+    gu = geometry(0, 17408, 5120, 3, unrounded=True)
+    for M in (1, 4, 5, 8, 32):
+        assert lib.trellis_scatter_workspace_bytes(ctypes.byref(gu), M, 0) == M * 128 * 5120 * 4, M
 
 
 def test_glue_validation(lib):

@@ -157,6 +157,27 @@ def test_scatter_unrounded_full_size(orc):
     _agreement(orc, got, out, out_rnd, "unrounded scatter full size")
 
 
+@pytest.mark.parametrize("M", [5, 16])
+def test_scatter_unrounded_default_splits(orc, M):
+    """splits = 0 under the unrounded contract is scatter.ts's 128 ranges at
+    every M (not the split-K rule's 8 of the rounded contract): the default
+    call equals the call with 128 splits bit for bit, leaves the 128 split
+    partials in the workspace, and is within the tolerance of the oracle."""
+    import torch
+    rows, cols, k = 4096, 5120, 3
+    p = synth.problem(0, M, rows, cols, k, seed=29)
+    d = _device(p)
+    need = tcq.trellis_scatter_workspace_bytes(d["g"], M, 0)
+    assert need == M * 128 * cols * 4
+    ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    got = tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], workspace=ws)
+    want = tcq.trellis_scatter(d["x"], d["codes"], d["scales"], d["lut"], d["g"], splits=128)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    w32, y, a, out, part, out_rnd, part_rnd = _oracle_axis0(orc, p, 128)
+    check_close(orc, host_bf16(got), y, a, f"unrounded scatter default splits M={M}")
+    _check_partials(orc, p, w32, ws, part, part_rnd, 128, f"unrounded scatter default splits M={M}")
+
+
 def test_rounded_paths_agree_with_their_own_oracle(orc):
     """The same agreement statistic for the default (rounded) contract on the
     FMA paths: the matvec and the M <= 2 scatter."""

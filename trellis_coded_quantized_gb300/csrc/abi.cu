@@ -88,7 +88,7 @@ trellis_status scatter_common(const void* x, int32_t M, const uint32_t* codes, c
     trellis_status st = check_geometry(g, 0, true);
     if (st != TRELLIS_OK) return st;
     if (M < 1 || M > 32 || splits < 0 || splits > 1024) return TRELLIS_ERR_SHAPE;
-    const int s = tcq::scatter_splits(g->rows, g->cols, M, splits);
+    const int s = tcq::scatter_splits(g->rows, g->cols, M, splits, (g->flags & TRELLIS_FLAG_UNROUNDED) != 0);
     if (!aligned16(x) || !aligned16(codes) || !aligned16(lut) || !aligned16(workspace) ||
         !aligned16(out))
         return TRELLIS_ERR_ALIGN;
@@ -236,7 +236,7 @@ trellis_status trellis_kv_decode_inverse256(const uint8_t* key_codes, const void
 size_t trellis_scatter_workspace_bytes(const trellis_geometry* g, int32_t M, int32_t splits) {
     if (check_geometry(g, -1, true) != TRELLIS_OK || M < 1 || M > 32 || splits < 0 || splits > 1024) return 0;
     const bool unr = (g->flags & TRELLIS_FLAG_UNROUNDED) != 0;
-    return ((size_t)M * (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits) * (size_t)g->cols +
+    return ((size_t)M * (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits, unr) * (size_t)g->cols +
             (size_t)tcq::scatter_fix_floats(M, unr)) * sizeof(float);
 }
 

@@ -641,7 +641,10 @@ extern "C" trellis_status trellis_scatter_noalloc(const void* x, int32_t M, cons
     if (!g) return TRELLIS_ERR_NULL;
     // invalid arguments give 0 here and are reported by trellis_scatter
     const size_t need = trellis_scatter_workspace_bytes(g, M, splits);
-    if (need > 0 && (size_t)M * (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits) * (size_t)g->cols >
+    if (need > 0 && (size_t)M *
+                        (size_t)tcq::scatter_splits(g->rows, g->cols, M, splits,
+                                                    (g->flags & TRELLIS_FLAG_UNROUNDED) != 0) *
+                        (size_t)g->cols >
                         kNoAllocPartialFloats)
         return TRELLIS_ERR_WORKSPACE;
     int dev = -1;
