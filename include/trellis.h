@@ -183,7 +183,12 @@ trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t*
  *              launcher (splitk-prefill.ts): with tilesM = ceil(M/32),
  *              tilesN = ceil(cols/32), tilesK = floor(rows/16) and
  *              ratio = max(1, floor(tilesK / (tilesM*tilesN))), the power of
- *              two at or above ratio, clamped to [2, 32] (8 at 17408 x 5120)
+ *              two at or above ratio, clamped to [2, 32] (8 at 17408 x 5120).
+ *              Speed: the rounded contract from 3 rows with fewer than 128
+ *              splits takes the tensor-core path, which spreads any split
+ *              count over every SM.  Every other case (up to 2 rows, 128 or
+ *              more splits, the unrounded contract) runs one CTA per split,
+ *              so fewer splits than SMs leave SMs idle.
  *   workspace  f32, at least trellis_scatter_workspace_bytes(g, M, splits) bytes,
  *              16-byte aligned; contents on entry do not matter.  On return
  *              it holds the partials P[m][s][c] (empty ranges hold zeros).
