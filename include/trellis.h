@@ -187,8 +187,9 @@ trellis_status trellis_gate_up_prefill(const void* x, int32_t M, const uint32_t*
  *              Speed: the rounded contract from 3 rows with fewer than 128
  *              splits takes the tensor-core path, which spreads any split
  *              count over every SM.  Every other case (up to 2 rows, 128 or
- *              more splits, the unrounded contract) runs one CTA per split,
- *              so fewer splits than SMs leave SMs idle.
+ *              more splits, the unrounded contract) runs one CTA per split
+ *              (up to 2 rows: per split and 5120 columns), so fewer splits
+ *              than SMs leave SMs idle.
  *   workspace  f32, at least trellis_scatter_workspace_bytes(g, M, splits) bytes,
  *              16-byte aligned; contents on entry do not matter.  On return
  *              it holds the partials P[m][s][c] (empty ranges hold zeros).
