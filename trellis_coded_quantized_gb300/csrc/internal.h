@@ -79,18 +79,20 @@ cudaError_t launch_gather_probe(const float* lut, int blocks, int iters, int rep
 constexpr int64_t kMatvecMaxCols = 640 * 32;
 
 // Split count of the scatter.  An explicit count is taken as given.  The
-// default is 128 for up to 4 activation rows (scatter.ts, SCATTER_SPLITS),
-// and 128 at every M under the unrounded contract: that contract is the
-// one of scatter.ts's balanced scatter kernels, which run SCATTER_SPLITS
-// ranges, while the rule below belongs to the rounded split-K prefill; and
-// its kernel from 3 rows runs one CTA per split, so 8 splits would leave
-// all but 8 SMs idle.  Otherwise, from 5 rows, it is the rule of the
-// split-K launcher (splitk-prefill.ts):
-// tiles of 32 activation rows and 32 output columns, 16-row K tiles,
-// ratio = max(1, floor(K tiles / (row tiles * column tiles))) and
-// splits = min(32, max(2, the power of two at or above ratio)).  At 17408 x
-// 5120 that is 8.  The rows of split s are [s*rp, min(rows, (s+1)*rp)) with
-// rp = ceil(rows/splits) for every count.
+// default:
+//   - 128 for up to 4 activation rows (scatter.ts, SCATTER_SPLITS);
+//   - 128 at every M under the unrounded contract.  That contract is the one
+//     of scatter.ts's balanced scatter kernels, which run SCATTER_SPLITS
+//     ranges; the rule below belongs to the rounded split-K prefill.  Its
+//     kernel from 3 rows runs one CTA per split, so 8 splits would leave all
+//     but 8 SMs idle;
+//   - otherwise, from 5 rows, the rule of the split-K launcher
+//     (splitk-prefill.ts): tiles of 32 activation rows and 32 output
+//     columns, 16-row K tiles, ratio = max(1, floor(K tiles / (row tiles *
+//     column tiles))) and splits = min(32, max(2, the power of two at or
+//     above ratio)).  At 17408 x 5120 that is 8.
+// The rows of split s are [s*rp, min(rows, (s+1)*rp)) with rp =
+// ceil(rows/splits) for every count.
 inline int scatter_splits(int64_t rows, int64_t cols, int M, int splits, bool unrounded) {
     if (splits != 0) return splits;
     if (M <= 4 || unrounded) return 128;
