@@ -269,6 +269,12 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
         const int row0 = 16 * ks + 4 * c;
         const int sw = c & 2;
         const int widx[3] = {wi, w1i, w2i};
+        // Byte offset of word widx[t] in tile row row0 + j, j = 0..3, is
+        // (wofs[t] ^ (j << 4)) + (j << 7): row0 is a multiple of 4, so the
+        // row's swizzle phase is (row0 & 7) | j and j only flips chunk bits.
+        uint32_t wofs[3];
+        #pragma unroll
+        for (int t = 0; t < 3; ++t) wofs[t] = ctile_off(row0, widx[t]);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t info_base = s_base + Lay::kInfoOff;
         const uint32_t scl_base = s_base + Lay::kSclOff;
@@ -295,7 +301,8 @@ scatter_tc_kernel(const uint16_t* __restrict__ x, int M, const uint32_t* __restr
                 #pragma unroll
                 for (int t = 0; t < 3; ++t) {
                     uint32_t v;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tile + ctile_off(row0 + (i ^ sw), widx[t])));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v)
+                                 : "r"(tile + ((wofs[t] ^ ((uint32_t)(i ^ sw) << 4)) + ((uint32_t)(i ^ sw) << 7))));
                     h.wv[i][t] = v;
                 }
             }
